@@ -1,0 +1,157 @@
+"""Thin ctypes binding of libbitdelta.so (C ABI in ``include/bitdelta.h``).
+
+Function names match the C entry points.  This module only marshals
+arguments: torch tensors become device pointers and sizes, the current torch
+CUDA stream is passed as the stream, and a non-zero status raises
+``BitDeltaError``.  Every step of the computation runs in the library's CUDA
+kernels; there is no fallback, and a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libbitdelta.so")
+
+BD_OK = 0
+BD_ERR_INVALID_ARG = 1
+BD_ERR_UNSUPPORTED_SHAPE = 2
+BD_ERR_MISALIGNED = 3
+BD_ERR_WORKSPACE = 4
+BD_ERR_CUDA = 5
+BD_ERR_DEVICE_TIMEOUT = 6
+BD_ERR_BAD_VARIANT_ID = 7
+BD_ALPHA_SCALAR = 0
+BD_ALPHA_PER_ROW = 1
+BD_MAX_VARIANTS = 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+class BitDeltaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {bd_status_string(status)} (status {status})")
+
+
+def load_library(path: str | None = None):
+    """Open libbitdelta.so (built by ``bit_delta_tenant_gb300.build``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libbitdelta.so not found at {p}; build it with "
+                               "`python -m bit_delta_tenant_gb300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(p)
+        V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.bd_version.restype = I32
+        lib.bd_status_string.argtypes = [I32]
+        lib.bd_status_string.restype = ctypes.c_char_p
+        lib.bd_set_wait_limit_ns.argtypes = [I64]
+        lib.bd_set_wait_limit_ns.restype = I64
+        lib.bd_set_linear_path.argtypes = [I32]
+        lib.bd_set_linear_path.restype = I32
+        lib.bd_get_device_status.argtypes = [V]
+        lib.bd_get_device_status.restype = I32
+        lib.bd_compress_workspace_size.argtypes = [I64, I64, I32]
+        lib.bd_compress_workspace_size.restype = SZ
+        lib.bd_compress.argtypes = [V, V, I64, I64, I32, V, V, V, SZ, V]
+        lib.bd_compress.restype = I32
+        lib.bd_linear.argtypes = [V, I64, V, V, V, I32, I64, I64, V, V]
+        lib.bd_linear.restype = I32
+        lib.bd_linear_grouped_workspace_size.argtypes = [I64, I32, I64, I64]
+        lib.bd_linear_grouped_workspace_size.restype = SZ
+        lib.bd_linear_grouped.argtypes = [V, V, I64, V, V, V, V, I32, I64, I64, V, V, SZ, V]
+        lib.bd_linear_grouped.restype = I32
+        _lib = lib
+        return lib
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream if hasattr(s, "cuda_stream") else int(s))
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libbitdelta must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != BD_OK:
+        raise BitDeltaError(rc, where)
+
+
+def bd_version() -> int:
+    return int(load_library().bd_version())
+
+
+def bd_status_string(status: int) -> str:
+    return load_library().bd_status_string(int(status)).decode()
+
+
+def bd_set_wait_limit_ns(limit_ns: int) -> int:
+    return int(load_library().bd_set_wait_limit_ns(int(limit_ns)))
+
+
+def bd_set_linear_path(path: int) -> int:
+    return int(load_library().bd_set_linear_path(int(path)))
+
+
+def bd_get_device_status(stream=None) -> int:
+    return int(load_library().bd_get_device_status(_stream(stream)))
+
+
+def bd_compress_workspace_size(n_out: int, n_in: int, alpha_mode: int) -> int:
+    return int(load_library().bd_compress_workspace_size(n_out, n_in, alpha_mode))
+
+
+def bd_compress(w_base: torch.Tensor, w_ft: torch.Tensor, alpha_mode: int, bits_out: torch.Tensor,
+                alpha_out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Packed sign bits and alpha of (W_base, W_ft); all tensors on the device."""
+    n_out, n_in = w_base.shape
+    rc = load_library().bd_compress(_ptr(w_base), _ptr(w_ft), n_out, n_in, int(alpha_mode), _ptr(bits_out),
+                                    _ptr(alpha_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check(rc, "bd_compress")
+
+
+def bd_linear(x: torch.Tensor, w_base: torch.Tensor, bits: torch.Tensor, alpha: torch.Tensor, alpha_mode: int,
+              y: torch.Tensor, stream=None) -> None:
+    """y[m, n_out] = x[m, n_in] . (W_base + alpha * sign)^T."""
+    m = x.shape[0] if x.dim() == 2 else 0
+    n_out, n_in = w_base.shape
+    rc = load_library().bd_linear(_ptr(x), m, _ptr(w_base), _ptr(bits), _ptr(alpha), int(alpha_mode), n_out, n_in,
+                                  _ptr(y), _stream(stream))
+    _check(rc, "bd_linear")
+
+
+def bd_linear_grouped_workspace_size(m: int, n_variants: int, n_out: int, n_in: int) -> int:
+    return int(load_library().bd_linear_grouped_workspace_size(m, n_variants, n_out, n_in))
+
+
+def bd_linear_grouped(x: torch.Tensor, variant_ids: torch.Tensor, w_base: torch.Tensor, bits_v, alpha_v,
+                      alpha_modes_v, y: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """Multi-tenant fused linear: token t uses (bits_v[ids[t]], alpha_v[ids[t]])."""
+    n_var = len(bits_v)
+    if len(alpha_v) != n_var or len(alpha_modes_v) != n_var:
+        raise ValueError("bits_v, alpha_v and alpha_modes_v must have one entry per variant")
+    m = x.shape[0]
+    n_out, n_in = w_base.shape
+    bits_arr = (ctypes.c_void_p * n_var)(*[b.data_ptr() for b in bits_v])
+    alpha_arr = (ctypes.c_void_p * n_var)(*[a.data_ptr() for a in alpha_v])
+    modes_arr = (ctypes.c_int32 * n_var)(*[int(md) for md in alpha_modes_v])
+    rc = load_library().bd_linear_grouped(_ptr(x), _ptr(variant_ids), m, _ptr(w_base), bits_arr, alpha_arr,
+                                          modes_arr, n_var, n_out, n_in, _ptr(y), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "bd_linear_grouped")

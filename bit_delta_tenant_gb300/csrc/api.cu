@@ -1,0 +1,259 @@
+// api.cu -- the extern "C" boundary of libbitdelta.so (declared in
+// include/bitdelta.h): argument validation before any launch, the sticky
+// device status word, the wait-limit knob, path dispatch for the fused
+// linear, and tensor-map encoding through the runtime's driver entry point
+// (so the library needs no link-time dependency on the driver library).
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "bd_internal.h"
+#include "bitdelta.h"
+
+#define BD_API extern "C" __attribute__((visibility("default")))
+
+// Sticky device status word (bits bd::kDevTimeout, bd::kDevBadVariant).  Kernels
+// receive its device address; the host reads and clears it in bd_get_device_status.
+__device__ unsigned int g_bd_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 128;
+std::mutex g_mu;
+unsigned *g_status_ptr[kMaxDevices] = {nullptr};
+int g_num_sms[kMaxDevices] = {0};
+std::atomic<int64_t> g_wait_ns{-1};
+std::atomic<int32_t> g_linear_path{0};
+
+int64_t wait_limit_ns() {
+    int64_t v = g_wait_ns.load();
+    if (v < 0) {
+        int64_t init = 2000000000LL;
+        if (const char *e = std::getenv("BD_WAIT_LIMIT_NS")) {
+            char *end = nullptr;
+            long long p = std::strtoll(e, &end, 10);
+            if (end != e && p >= 0) init = p;
+        }
+        int64_t expected = -1;
+        g_wait_ns.compare_exchange_strong(expected, init);
+        v = g_wait_ns.load();
+    }
+    return v;
+}
+
+int32_t make_ctx(bd::DevCtx *ctx) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BD_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (g_status_ptr[dev] == nullptr) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_bd_status_word) != cudaSuccess) return BD_ERR_CUDA;
+            int sms = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BD_ERR_CUDA;
+            g_status_ptr[dev] = static_cast<unsigned *>(p);
+            g_num_sms[dev] = sms;
+        }
+        ctx->status = g_status_ptr[dev];
+        ctx->num_sms = g_num_sms[dev];
+    }
+    ctx->device = dev;
+    ctx->wait_ns = static_cast<uint64_t>(wait_limit_ns());
+    return BD_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int32_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return BD_OK;
+    return BD_ERR_CUDA;
+}
+
+int32_t check_matrix_shape(int64_t n_out, int64_t n_in) {
+    if (n_out < 1 || n_in < 1) return BD_ERR_INVALID_ARG;
+    if (n_in % 8 != 0) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (n_out >= BD_MAX_DIM || n_in >= BD_MAX_DIM) return BD_ERR_UNSUPPORTED_SHAPE;
+    return BD_OK;
+}
+
+}  // namespace
+
+namespace bd {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                          uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace bd
+
+BD_API int32_t bd_version(void) { return 100; }
+
+BD_API const char *bd_status_string(int32_t status) {
+    switch (status) {
+        case BD_OK: return "ok";
+        case BD_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive size or unknown mode)";
+        case BD_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (n_in must be a multiple of 8; sizes below 2^31)";
+        case BD_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        case BD_ERR_WORKSPACE: return "workspace missing or too small";
+        case BD_ERR_CUDA: return "CUDA runtime error";
+        case BD_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+        case BD_ERR_BAD_VARIANT_ID: return "variant id outside [0, n_variants)";
+        default: return "unknown status";
+    }
+}
+
+BD_API int64_t bd_set_wait_limit_ns(int64_t limit_ns) {
+    const int64_t prev = wait_limit_ns();
+    if (limit_ns >= 0) g_wait_ns.store(limit_ns);
+    return prev;
+}
+
+BD_API int32_t bd_set_linear_path(int32_t path) {
+    const int32_t prev = g_linear_path.load();
+    if (path >= 0 && path <= 2) g_linear_path.store(path);
+    return prev;
+}
+
+BD_API int32_t bd_get_device_status(void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return BD_ERR_CUDA;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_bd_status_word, sizeof(word)) != cudaSuccess) return BD_ERR_CUDA;
+    const unsigned zero = 0;
+    if (word != 0 && cudaMemcpyToSymbol(g_bd_status_word, &zero, sizeof(zero)) != cudaSuccess) return BD_ERR_CUDA;
+    if (word & bd::kDevTimeout) return BD_ERR_DEVICE_TIMEOUT;
+    if (word & bd::kDevBadVariant) return BD_ERR_BAD_VARIANT_ID;
+    return BD_OK;
+}
+
+// ---------------------------------------------------------------- compression
+
+BD_API size_t bd_compress_workspace_size(int64_t n_out, int64_t n_in, int32_t alpha_mode) {
+    if (check_matrix_shape(n_out, n_in) != BD_OK) return 0;
+    if (alpha_mode != BD_ALPHA_SCALAR && alpha_mode != BD_ALPHA_PER_ROW) return 0;
+    const bd::CompressGeom g = bd::compress_geometry(n_out, n_in, alpha_mode);
+    return static_cast<size_t>(g.rows * g.segs) * sizeof(double);
+}
+
+BD_API int32_t bd_compress(const void *w_base, const void *w_ft, int64_t n_out, int64_t n_in, int32_t alpha_mode,
+                           uint8_t *bits_out, float *alpha_out, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    if (!w_base || !w_ft || !bits_out || !alpha_out) return BD_ERR_INVALID_ARG;
+    if (alpha_mode != BD_ALPHA_SCALAR && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    const int32_t shape = check_matrix_shape(n_out, n_in);
+    if (shape != BD_OK) return shape;
+    if (!aligned16(w_base) || !aligned16(w_ft) || !aligned16(bits_out) || !aligned16(alpha_out))
+        return BD_ERR_MISALIGNED;
+    const size_t need = bd_compress_workspace_size(n_out, n_in, alpha_mode);
+    if (workspace == nullptr || workspace_bytes < need) return BD_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return BD_ERR_MISALIGNED;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    return cuda_status(bd::launch_compress(w_base, w_ft, n_out, n_in, alpha_mode, bits_out, alpha_out,
+                                           static_cast<double *>(workspace), ctx,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- fused linear
+
+BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                         int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, void *stream) {
+    if (m < 0) return BD_ERR_INVALID_ARG;
+    if (!w_base || !bits || !alpha) return BD_ERR_INVALID_ARG;
+    if (m > 0 && (!x || !y)) return BD_ERR_INVALID_ARG;
+    if (alpha_mode != BD_ALPHA_SCALAR && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    const int32_t shape = check_matrix_shape(n_out, n_in);
+    if (shape != BD_OK) return shape;
+    if (m >= BD_MAX_DIM) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(w_base) || !aligned16(bits) || !aligned16(alpha)) return BD_ERR_MISALIGNED;
+    if (m > 0 && (!aligned16(x) || !aligned16(y))) return BD_ERR_MISALIGNED;
+    if (m == 0) return BD_OK;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int32_t path = g_linear_path.load();
+    const bool decode_ok = bd::decode_supported(m, n_out, n_in, ctx.num_sms);
+    bool use_decode = decode_ok && m <= bd::kDecodeMaxM;
+    if (path == 1) {
+        if (!decode_ok) return BD_ERR_UNSUPPORTED_SHAPE;
+        use_decode = true;
+    } else if (path == 2) {
+        use_decode = false;
+    }
+    if (use_decode)
+        return cuda_status(bd::launch_decode(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));
+    return cuda_status(bd::launch_prefill(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));
+}
+
+// ---------------------------------------------------------------- multi-tenant
+
+BD_API size_t bd_linear_grouped_workspace_size(int64_t m, int32_t n_variants, int64_t n_out, int64_t n_in) {
+    if (m < 0 || n_variants < 1 || n_variants > BD_MAX_VARIANTS) return 0;
+    if (check_matrix_shape(n_out, n_in) != BD_OK) return 0;
+    return bd::grouped_workspace_size(m, n_variants, n_out, n_in);
+}
+
+BD_API int32_t bd_linear_grouped(const void *x, const int32_t *variant_ids, int64_t m, const void *w_base,
+                                 const uint8_t *const *bits_v, const float *const *alpha_v,
+                                 const int32_t *alpha_modes_v, int32_t n_variants, int64_t n_out, int64_t n_in,
+                                 void *y, void *workspace, size_t workspace_bytes, void *stream) {
+    if (m < 0 || !w_base || !bits_v || !alpha_v || !alpha_modes_v) return BD_ERR_INVALID_ARG;
+    if (n_variants < 1 || n_variants > BD_MAX_VARIANTS) return BD_ERR_INVALID_ARG;
+    if (m > 0 && (!x || !y || !variant_ids)) return BD_ERR_INVALID_ARG;
+    const int32_t shape = check_matrix_shape(n_out, n_in);
+    if (shape != BD_OK) return shape;
+    if (m >= BD_MAX_DIM) return BD_ERR_UNSUPPORTED_SHAPE;
+    bd::GroupedVariants vars;
+    vars.count = n_variants;
+    for (int v = 0; v < n_variants; ++v) {
+        if (!bits_v[v] || !alpha_v[v]) return BD_ERR_INVALID_ARG;
+        if (alpha_modes_v[v] != BD_ALPHA_SCALAR && alpha_modes_v[v] != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+        if (!aligned16(bits_v[v]) || !aligned16(alpha_v[v])) return BD_ERR_MISALIGNED;
+        vars.bits[v] = bits_v[v];
+        vars.alpha[v] = alpha_v[v];
+        vars.mode[v] = alpha_modes_v[v];
+    }
+    if (!aligned16(w_base)) return BD_ERR_MISALIGNED;
+    if (m > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(variant_ids))) return BD_ERR_MISALIGNED;
+    if (m == 0) return BD_OK;
+    const size_t need = bd::grouped_workspace_size(m, n_variants, n_out, n_in);
+    if (workspace == nullptr || workspace_bytes < need) return BD_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return BD_ERR_MISALIGNED;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    return cuda_status(bd::launch_grouped(x, variant_ids, m, w_base, vars, n_out, n_in, y, workspace,
+                                          workspace_bytes, ctx, static_cast<cudaStream_t>(stream)));
+}

@@ -1,0 +1,73 @@
+// bd_internal.h -- host-side interfaces between the C-ABI layer (api.cu) and
+// the kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bd {
+
+// Bits of the sticky device status word (set with atomicOr by kernels, read
+// and cleared by the host).
+constexpr unsigned kDevTimeout = 1u;
+constexpr unsigned kDevBadVariant = 2u;
+
+// Per-launch context every kernel receives: where to record device-side
+// errors, and the wall-clock limit of bounded waits.
+struct DevCtx {
+    unsigned *status;     // device address of the sticky status word
+    uint64_t wait_ns;     // limit of every bounded wait
+    int num_sms;          // SM count of the current device
+    int device;           // current device ordinal
+};
+
+// ---- compression -------------------------------------------------------------------
+constexpr int kCompressThreads = 256;
+constexpr int kCompressChunksPerThread = 8;                                        // 16-byte chunks
+constexpr int64_t kCompressChunksPerSeg = kCompressThreads * kCompressChunksPerThread;  // 2048 chunks
+
+// Geometry of the deterministic two-level reduction: `rows` independent sums
+// (1 for a scalar alpha, n_out per-row), each over `row_chunks` chunks of 8
+// elements split into `segs` fixed segments.
+struct CompressGeom {
+    int64_t rows, row_chunks, segs;
+};
+CompressGeom compress_geometry(int64_t n_out, int64_t n_in, int32_t alpha_mode);
+
+cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out, int64_t n_in, int32_t alpha_mode,
+                            uint8_t *bits, float *alpha, double *partials, const DevCtx &ctx, cudaStream_t stream);
+
+// ---- fused linear ---------------------------------------------------------------------
+// HBM-streaming small-m kernel (m <= kDecodeMaxM).  Returns cudaErrorNotSupported
+// if the activation slice does not fit in shared memory (caller falls back).
+constexpr int kDecodeMaxM = 64;
+bool decode_supported(int64_t m, int64_t n_out, int64_t n_in, int num_sms);
+cudaError_t launch_decode(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                          int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                          cudaStream_t stream);
+
+// Tensor-core (tcgen05 + TMA) kernel for any m.
+cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                           int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                           cudaStream_t stream);
+
+// ---- multi-tenant ----------------------------------------------------------------------
+struct GroupedVariants {
+    const uint8_t *bits[64];
+    const float *alpha[64];
+    int32_t mode[64];
+    int32_t count;
+};
+size_t grouped_workspace_size(int64_t m, int32_t n_variants, int64_t n_out, int64_t n_in);
+cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const void *w_base,
+                           const GroupedVariants &vars, int64_t n_out, int64_t n_in, void *y, void *ws,
+                           size_t ws_bytes, const DevCtx &ctx, cudaStream_t stream);
+
+// ---- driver entry point for tensor maps (resolved through the runtime) ---------------
+bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+                          uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle);
+
+}  // namespace bd

@@ -1,0 +1,309 @@
+// prefill.cu -- fused BitDelta linear for large token counts on the 5th
+// generation tensor cores: y = x . (W_base + alpha*S)^T with W_eff rebuilt
+// tile by tile in shared memory and never written to HBM.
+//
+// Method: "BitDelta : servir 14 modèles Zen depuis un seul cluster GPU"
+// (Hanzo blog), section "Architecture de service": the effective weight is
+// rebuilt on the fly by a fused kernel that reads the base weights and the
+// delta bits together, in registers or shared memory, and the reconstruction
+// is fused with the matrix multiply (conceptual fused_bitdelta_linear
+// listing: unpack to {-1,+1}, W_eff = W_base + alpha*unpacked, linear).
+//
+// One CTA computes a 128 (W rows) x 256 (tokens) tile of y^T:
+//   warp 0      TMA producer: per 64-wide K block, the W_base tile
+//               [128 x 64] and the x tile [256 x 64], both K-major with the
+//               128-byte swizzle, into a 4-stage ring.
+//   warps 2..5  reconstruction: thread r owns tile row r; it reads the row's
+//               8 packed bytes for the K block (prefetched two blocks ahead),
+//               and rewrites each 16-byte chunk of the swizzled W tile in
+//               place as bf16(fp32(W_base) + alpha_r * s) -- one chunk is
+//               exactly one packed byte.  After the K loop the same warps are
+//               the epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+//   warp 1      allocates 256 TMEM columns; lane 0 issues
+//               tcgen05.mma kind::f16 (M=128, N=256, K=16, bf16 in, fp32
+//               accumulate in TMEM) on the reconstructed tile and commits
+//               each stage back to the producer.
+// Every wait is bounded; a role that gives up records a timeout in the status
+// word, tells the other roles through a shared flag, drains its own copies
+// and MMAs in flight, and the CTA frees its TMEM and returns.
+#include "bd_device.cuh"
+#include "bd_internal.h"
+
+namespace bd {
+namespace {
+
+constexpr int kBM = 128;  // W rows per tile (MMA M)
+constexpr int kBN = 256;  // tokens per tile (MMA N)
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr uint32_t kWBytes = kBM * kBK * 2;
+constexpr uint32_t kXBytes = kBN * kBK * 2;
+constexpr uint32_t kStageTx = kWBytes + kXBytes;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+constexpr size_t kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 256;
+
+struct PrefillArgs {
+    const uint8_t *bits;
+    const float *alpha;
+    uint16_t *y;
+    int64_t m, n_out, n_in;
+    int32_t mode;
+    int32_t num_kb;
+    int32_t row_tiles, tok_tiles, group;
+    int32_t bits_vec8;  // rows of packed bits are 8-byte aligned
+    unsigned *status;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ uint32_t rebuild_pair(uint32_t w, uint32_t byte, int i, float al) {
+    const float lo = bf16lo_to_f32(w) + (((byte >> (2 * i)) & 1u) ? al : -al);
+    const float hi = bf16hi_to_f32(w) + (((byte >> (2 * i + 1)) & 1u) ? al : -al);
+    return pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *status) {
+    *abort_flag = 1;
+    flag_status(status, kDevTimeout);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                   PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sW = smem;
+    uint8_t *sX = smem + kStages * kWBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sX + kStages * kXBytes);
+    uint64_t *full = bars;
+    uint64_t *rebuilt = bars + kStages;
+    uint64_t *empty = bars + 2 * kStages;
+    uint64_t *acc_full = bars + 3 * kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    // Grouped rasterisation: consecutive CTAs cycle over `group` token tiles
+    // for one W tile, so a wave touches a compact block of W and x in L2.
+    const int tile = blockIdx.x;
+    const int per_group = a.group * a.row_tiles;
+    const int grp = tile / per_group;
+    const int rem = tile - grp * per_group;
+    const int gsize = min(a.group, a.tok_tiles - grp * a.group);
+    const int tok_tile = grp * a.group + rem % gsize;
+    const int row_tile = rem / gsize;
+    const int m0 = row_tile * kBM;
+    const int n0 = tok_tile * kBN;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nkb = a.num_kb;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&rebuilt[s], 4);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (kb / kStages) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1, a.wait_ns, abort_flag)) {
+                    give_up(abort_flag, a.status);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], kStageTx);
+                tma_load_2d(sW + s * kWBytes, &tm_w, &full[s], kb * kBK, m0);
+                tma_load_2d(sX + s * kXBytes, &tm_x, &full[s], kb * kBK, n0);
+                issued = kb + 1;
+            }
+            if (*abort_flag) {
+                // Drain: the loads of the last stages issued must land before the CTA exits.
+                for (int kb = (issued > kStages ? issued - kStages : 0); kb < issued; ++kb)
+                    mbar_wait(&full[kb % kStages], (kb / kStages) & 1, kDrainLimitNs, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+            bool ok = true;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (kb / kStages) & 1;
+                if (!mbar_wait(&rebuilt[s], ph, a.wait_ns, abort_flag)) {
+                    give_up(abort_flag, a.status);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sW + s * kWBytes);
+                const uint32_t b_addr = smem_u32(sX + s * kXBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    tc_mma_f16_ss(tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32),
+                                  idesc, (kb | kk) != 0 ? 1u : 0u);
+                }
+                tc_commit(&empty[s]);
+            }
+            // Always wait for this thread's MMAs before the CTA may free TMEM, even if
+            // the epilogue gave up early (its wait can run out while MMAs still run).
+            tc_commit(acc_full);
+            (void)ok;
+            mbar_wait(acc_full, 0, kDrainLimitNs, nullptr);
+        }
+    } else {
+        // ---- reconstruction (then epilogue) warps --------------------------------------
+        const int sub = warp & 3;  // TMEM lane quarter this warp may access
+        const int r = sub * 32 + lane;
+        const int64_t row = static_cast<int64_t>(m0) + r;
+        const bool row_ok = row < a.n_out;
+        const float al = row_ok ? (a.mode ? a.alpha[row] : a.alpha[0]) : 0.0f;
+        const int64_t bpr = a.n_in / 8;
+        const uint8_t *brow = a.bits + (row_ok ? row : 0) * bpr;
+
+        auto load_bits = [&](int kb) -> uint2 {
+            uint2 v = make_uint2(0u, 0u);
+            if (row_ok && kb < nkb) {
+                const int64_t c0 = static_cast<int64_t>(kb) * 8;
+                if (a.bits_vec8 && c0 + 8 <= bpr) {
+                    v = __ldg(reinterpret_cast<const uint2 *>(brow + c0));
+                } else {
+                    uint32_t lo = 0, hi = 0;
+                    for (int c = 0; c < 8; ++c) {
+                        if (c0 + c < bpr) {
+                            const uint32_t b = __ldg(brow + c0 + c);
+                            if (c < 4) lo |= b << (8 * c);
+                            else hi |= b << (8 * (c - 4));
+                        }
+                    }
+                    v = make_uint2(lo, hi);
+                }
+            }
+            return v;
+        };
+
+        uint2 b_cur = load_bits(0);
+        uint2 b_nxt = load_bits(1);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+            const int s = kb % kStages;
+            const uint32_t ph = (kb / kStages) & 1;
+            const uint2 b_nn = load_bits(kb + 2);
+            const bool got = mbar_wait(&full[s], ph, a.wait_ns, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                if (lane == 0) give_up(abort_flag, a.status);
+                ok = false;
+                break;
+            }
+            uint8_t *rowp = sW + s * kWBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t byte = ((c < 4 ? b_cur.x : b_cur.y) >> (8 * (c & 3))) & 0xFFu;
+                uint4 *p = reinterpret_cast<uint4 *>(rowp + ((c ^ (r & 7)) << 4));
+                uint4 w = *p;
+                w.x = rebuild_pair(w.x, byte, 0, al);
+                w.y = rebuild_pair(w.y, byte, 1, al);
+                w.z = rebuild_pair(w.z, byte, 2, al);
+                w.w = rebuild_pair(w.w, byte, 3, al);
+                *p = w;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rebuilt[s]);
+            b_cur = b_nxt;
+            b_nxt = b_nn;
+        }
+
+        if (ok) {
+            const bool got = mbar_wait(acc_full, 0, a.wait_ns, abort_flag);
+            if (__all_sync(0xFFFFFFFFu, got)) {
+                tc_fence_after();
+                const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+                uint16_t *ycol = a.y + row;
+#pragma unroll 1
+                for (int c0 = 0; c0 < kBN; c0 += 32) {
+                    if (n0 + c0 >= a.m) break;  // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(lane_addr + c0, v);
+                    tmem_ld_wait();
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int64_t t = static_cast<int64_t>(n0) + c0 + i;
+                            if (t < a.m) {
+                                __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[i]));
+                                ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&h);
+                            }
+                        }
+                    }
+                }
+            } else if (lane == 0) {
+                give_up(abort_flag, a.status);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                           int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                           cudaStream_t stream) {
+    static bool attr_set[128] = {false};
+    if (ctx.device < 128 && !attr_set[ctx.device]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_set[ctx.device] = true;
+    }
+    CUtensorMap tm_w, tm_x;
+    if (!encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kBK, kBM,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, m, n_in * 2, kBK, kBN,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    PrefillArgs a;
+    a.bits = bits;
+    a.alpha = alpha;
+    a.y = static_cast<uint16_t *>(y);
+    a.m = m;
+    a.n_out = n_out;
+    a.n_in = n_in;
+    a.mode = alpha_mode;
+    a.num_kb = static_cast<int32_t>((n_in + kBK - 1) / kBK);
+    a.row_tiles = static_cast<int32_t>((n_out + kBM - 1) / kBM);
+    a.tok_tiles = static_cast<int32_t>((m + kBN - 1) / kBN);
+    a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
+    a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
+    const int64_t tiles = static_cast<int64_t>(a.row_tiles) * a.tok_tiles;
+    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    prefill_kernel<<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+    return cudaGetLastError();
+}
+
+}  // namespace bd

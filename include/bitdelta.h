@@ -1,0 +1,192 @@
+/*
+ * bitdelta.h -- C ABI of libbitdelta.so, the GB300 (sm_103a) BitDelta hot path.
+ *
+ * BitDelta stores a fine-tuned weight matrix as the shared base W_base plus a
+ * 1-bit delta: W_ft ~= W_base + alpha * sign(W_ft - W_base).  Method source:
+ * the blog page "BitDelta : servir 14 modèles Zen depuis un seul cluster GPU"
+ * (Hanzo blog); sections cited below:
+ *   [math]  "Le fondement mathématique"  Delta = W_ft - W_base; the 1-bit
+ *           approximation W_base + alpha*sign(Delta); alpha = mean|Delta|.
+ *   [serve] "Architecture de service"    W_eff is rebuilt on the fly inside one
+ *           fused kernel that reads W_base and the packed bits together and
+ *           never writes W_eff to HBM; the conceptual fused_bitdelta_linear
+ *           listing (x [batch, seq, d_in], W_base [d_out, d_in], packed signs,
+ *           alpha [d_out] or scalar, result = linear(x, W_eff)).
+ *   [infra] "Détails d'infrastructure"   signs packed 8 per byte
+ *           (4096x4096 -> 4096x512); alpha stored as fp32, one per output row.
+ *
+ * Conventions shared by every entry point
+ *   - Shapes use n_out = d_out (rows of W) and n_in = d_in (columns).  All
+ *     matrices are dense row-major.  bf16 tensors are passed as void*.
+ *   - x [batch, seq, d_in] is flattened by the caller to [m, n_in].
+ *   - Packed bits [n_out, n_in/8] (uint8): bit i of byte c in row j is the
+ *     sign of element k = 8c + i (least significant bit = lowest d_in);
+ *     bit = 1 iff Delta >= 0 (zero deltas, either sign of zero, pack as 1)
+ *     and unpacks to +1, bit 0 to -1.  The page prints neither the bit order
+ *     nor sign(0); these are the readings this library fixes.
+ *   - Every pointer is a DEVICE pointer unless marked "host".  The caller
+ *     allocates and owns every buffer (inputs, outputs and workspace); the
+ *     library allocates nothing, frees nothing and keeps no pointer after a
+ *     call returns.
+ *   - Every device pointer must be 16-byte aligned; n_in must be a multiple of
+ *     8 (one packed byte per 8 inputs).  Any n_in that is a multiple of 8, any
+ *     n_out >= 1 and any m >= 0 are handled on the GPU (ragged tails included).
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL =
+ *     the legacy default stream).  Argument errors are returned synchronously
+ *     before anything is launched.  Device-side errors (a variant id out of
+ *     range, a bounded wait that ran out) are recorded in a sticky per-process
+ *     device status word and reported by bd_get_device_status().
+ *   - Calls are safe from several host threads on different streams; two
+ *     calls must not write the same output or workspace concurrently.
+ */
+#ifndef BITDELTA_H
+#define BITDELTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes of every entry point. */
+typedef enum bd_status {
+    BD_OK = 0,
+    BD_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad mode      */
+    BD_ERR_UNSUPPORTED_SHAPE = 2, /* n_in % 8 != 0, sizes beyond the limits     */
+    BD_ERR_MISALIGNED = 3,        /* a device pointer is not 16-byte aligned    */
+    BD_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required */
+    BD_ERR_CUDA = 5,              /* a CUDA runtime call failed                 */
+    BD_ERR_DEVICE_TIMEOUT = 6,    /* a bounded device-side wait ran out         */
+    BD_ERR_BAD_VARIANT_ID = 7     /* a variant id outside [0, n_variants)       */
+} bd_status;
+
+/* How alpha is stored ([math]: one per matrix; [infra]: one per output row). */
+typedef enum bd_alpha_mode {
+    BD_ALPHA_SCALAR = 0,  /* alpha: 1 float,     alpha   = mean_{j,k} |Delta_jk| */
+    BD_ALPHA_PER_ROW = 1  /* alpha: n_out floats, alpha_j = mean_k |Delta_jk|    */
+} bd_alpha_mode;
+
+/* Upper limits checked on entry. */
+#define BD_MAX_VARIANTS 64          /* variants per bd_linear_grouped call */
+#define BD_MAX_DIM ((int64_t)1 << 31) /* n_out, n_in and m are each below this */
+
+/* ------------------------------------------------------------------------ *
+ * Compression  ([math] Delta, sign, alpha; [infra] packing and fp32 alpha)
+ *
+ * Delta = fp32(W_ft) - fp32(W_base) element-wise (the subtraction is done in
+ * fp32 from the bf16 inputs).  Writes the packed sign bits and alpha:
+ *   scalar:  alpha[0] = sum_{j,k} |Delta_jk| / (n_out * n_in)
+ *   per-row: alpha[j] = sum_k |Delta_jk| / n_in
+ * The sums use fp32 partials over 8 elements, widened to fp64 and reduced
+ * in a fixed order, so alpha is bitwise reproducible for a given
+ * shape, and is rounded once to fp32 at the end.
+ *
+ *   w_base, w_ft  bf16 [n_out, n_in]   (read)
+ *   bits_out      uint8 [n_out, n_in/8] (written)
+ *   alpha_out     float [1] or [n_out]  (written)
+ *   workspace     device scratch of at least
+ *                 bd_compress_workspace_size(n_out, n_in, alpha_mode) bytes;
+ *                 its contents on entry are ignored.
+ * Errors: BD_ERR_INVALID_ARG, BD_ERR_UNSUPPORTED_SHAPE, BD_ERR_MISALIGNED,
+ *         BD_ERR_WORKSPACE, BD_ERR_CUDA (launch failure).
+ * ------------------------------------------------------------------------ */
+size_t bd_compress_workspace_size(int64_t n_out, int64_t n_in, int32_t alpha_mode);
+
+int32_t bd_compress(const void *w_base, const void *w_ft, int64_t n_out,
+                    int64_t n_in, int32_t alpha_mode, uint8_t *bits_out,
+                    float *alpha_out, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Fused linear  ([serve] fused reconstruction + matmul, never materialising
+ * W_eff in HBM; the conceptual fused_bitdelta_linear listing)
+ *
+ *   y[t, j] = sum_k x[t, k] * (W_base[j, k] + alpha_(j) * s_jk),
+ *   s_jk = +1 if bit(j, k) else -1, alpha_(j) = alpha[0] or alpha[j].
+ * Accumulation is fp32; y is rounded once to bf16.  Small m streams W_base
+ * and the bits from HBM once; large m runs a tensor-core (tcgen05) kernel
+ * that rebuilds each W tile in shared memory as bf16(W_base + alpha*s).
+ *
+ *   x       bf16 [m, n_in]      (read; m may be 0, then nothing is launched)
+ *   w_base  bf16 [n_out, n_in]  (read)
+ *   bits    uint8 [n_out, n_in/8] (read)
+ *   alpha   float [1] or [n_out] (read)
+ *   y       bf16 [m, n_out]     (written)
+ * Errors: BD_ERR_INVALID_ARG, BD_ERR_UNSUPPORTED_SHAPE, BD_ERR_MISALIGNED,
+ *         BD_ERR_CUDA; BD_ERR_DEVICE_TIMEOUT later via bd_get_device_status.
+ * ------------------------------------------------------------------------ */
+int32_t bd_linear(const void *x, int64_t m, const void *w_base,
+                  const uint8_t *bits, const float *alpha, int32_t alpha_mode,
+                  int64_t n_out, int64_t n_in, void *y, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Multi-tenant fused linear  ([serve]: many fine-tuned variants share one
+ * resident W_base; each request uses its own variant's packed delta)
+ *
+ * Token t uses variant v = variant_ids[t]:
+ *   y[t, j] = sum_k x[t, k] * (W_base[j, k] + alpha_v(j) * s^v_jk).
+ * Tokens are counting-sorted by variant on the device (stable), each
+ * variant's segment runs against the shared W_base, and y is written back in
+ * the ORIGINAL token order.  Variants with no tokens cost nothing.
+ *
+ *   x              bf16 [m, n_in]            (read)
+ *   variant_ids    int32 [m]                 (read, device)
+ *   w_base         bf16 [n_out, n_in]        (read)
+ *   bits_v         host array [n_variants] of device pointers, each
+ *                  uint8 [n_out, n_in/8]
+ *   alpha_v        host array [n_variants] of device pointers, each float
+ *                  [1] or [n_out] per alpha_modes_v
+ *   alpha_modes_v  host array [n_variants] of bd_alpha_mode values
+ *   n_variants     1 .. BD_MAX_VARIANTS
+ *   y              bf16 [m, n_out]           (written)
+ *   workspace      device scratch of at least
+ *                  bd_linear_grouped_workspace_size(m, n_variants, n_out, n_in)
+ * An id outside [0, n_variants) sets BD_ERR_BAD_VARIANT_ID in the device
+ * status word; the rows of y for such tokens are left unwritten.
+ * ------------------------------------------------------------------------ */
+size_t bd_linear_grouped_workspace_size(int64_t m, int32_t n_variants,
+                                        int64_t n_out, int64_t n_in);
+
+int32_t bd_linear_grouped(const void *x, const int32_t *variant_ids, int64_t m,
+                          const void *w_base, const uint8_t *const *bits_v,
+                          const float *const *alpha_v,
+                          const int32_t *alpha_modes_v, int32_t n_variants,
+                          int64_t n_out, int64_t n_in, void *y, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Status and debugging
+ * ------------------------------------------------------------------------ */
+
+/* Static English text for a status code (never NULL). */
+const char *bd_status_string(int32_t status);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device: BD_OK, BD_ERR_DEVICE_TIMEOUT or BD_ERR_BAD_VARIANT_ID (the
+ * first recorded, timeouts first).  BD_ERR_CUDA if the sync itself fails. */
+int32_t bd_get_device_status(void *stream);
+
+/* Debug knob: wall-clock limit, in nanoseconds, of every bounded device-side
+ * wait (mbarrier and pipeline waits) in kernels launched afterwards by this
+ * process.  Default 2e9 (2 s).  0 makes any wait that is not already
+ * satisfied give up at once; the kernel then records BD_ERR_DEVICE_TIMEOUT,
+ * drains its own copies in flight and returns.  Returns the previous value. */
+int64_t bd_set_wait_limit_ns(int64_t limit_ns);
+
+/* Debug knob: which fused-linear kernel later bd_linear calls use.
+ * 0 = automatic (the HBM-streaming kernel for m <= 64 when its activation
+ * slice fits in shared memory, the tensor-core kernel otherwise); 1 = always
+ * the streaming kernel (BD_ERR_UNSUPPORTED_SHAPE where it cannot run);
+ * 2 = always the tensor-core kernel.  Other values are ignored.  Returns the
+ * previous value. */
+int32_t bd_set_linear_path(int32_t path);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t bd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITDELTA_H */

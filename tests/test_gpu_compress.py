@@ -1,0 +1,109 @@
+"""GPU compression (bd_compress) against the fp64 oracle: packed bits bit-exact,
+alpha within 1e-6 relative, bitwise-reproducible alpha, on the workload shapes
+and on ragged shapes."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_delta_tenant_gb300 import bitdelta as bd
+from bit_delta_tenant_gb300 import synth, workloads
+from helpers import ALPHA_REL
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gpu_compress(w_base, w_ft, mode):
+    n_out, n_in = w_base.shape
+    bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=w_base.device)
+    alpha = torch.empty((n_out if mode == 1 else 1,), dtype=torch.float32, device=w_base.device)
+    ws = torch.empty((max(1, bd.bd_compress_workspace_size(n_out, n_in, mode)),), dtype=torch.uint8,
+                     device=w_base.device)
+    bd.bd_compress(w_base, w_ft, mode, bits, alpha, ws)
+    torch.cuda.synchronize()
+    return bits, alpha
+
+
+def check_against_oracle(w_base, w_ft, mode):
+    bits, alpha = gpu_compress(w_base, w_ft, mode)
+    wb, wf = synth.as_u16(w_base), synth.as_u16(w_ft)
+    ref_bits = oracle.sign_bits(wb, wf)
+    got = bits.cpu().numpy()
+    if not np.array_equal(got, ref_bits):
+        bad = np.argwhere(got != ref_bits)
+        raise AssertionError(f"{len(bad)} packed bytes differ; first at {tuple(bad[0])}")
+    a64 = oracle.alpha(wb, wf, mode)
+    a32 = alpha.cpu().numpy().astype(np.float64)
+    rel = np.abs(a32 - a64) / np.abs(a64)
+    assert rel.max() <= ALPHA_REL, f"alpha relative error {rel.max():.3e}"
+    return bits, alpha
+
+
+def _read_cases():
+    with open(os.path.join(GOLDEN, "sign_bytes.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield [p.strip() for p in line.split(";")]
+
+
+@pytest.mark.parametrize("case", list(_read_cases()), ids=lambda c: c[0])
+def test_hand_worked_bytes_on_gpu(case):
+    """The page-derived golden bytes, straight through the GPU kernel."""
+    _, rows, cols, wb, wf, expect = case
+    rows, cols = int(rows), int(cols)
+    wb = np.array([int(h, 16) for h in wb.split(",")], np.uint16).reshape(rows, cols)
+    wf = np.array([int(h, 16) for h in wf.split(",")], np.uint16).reshape(rows, cols)
+    expect = np.array([int(h, 16) for h in expect.split(",")], np.uint8).reshape(rows, cols // 8)
+    bits, _ = gpu_compress(synth.from_u16(wb, "cuda"), synth.from_u16(wf, "cuda"), 0)
+    assert np.array_equal(bits.cpu().numpy(), expect)
+
+
+@pytest.mark.parametrize("n_out,n_in", [(1, 8), (7, 24), (33, 120), (129, 136), (128, 4096), (3, 16392)])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_ragged_shapes(n_out, n_in, mode):
+    w_base, w_ft = synth.matrix_pair(n_out, n_in, 0.02, 1e-3, seed=n_out * 31 + n_in, device="cuda")
+    check_against_oracle(w_base, w_ft, mode)
+
+
+def test_tiny_workload():
+    c = workloads.TINY
+    w_base, w_ft = synth.matrix_pair(c["n_out"], c["n_in"], c["sigma"], c["b"], c["seed"], "cuda")
+    check_against_oracle(w_base, w_ft, c["mode"])
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA7B_LAYER["matrices"])))
+def test_llama7b_layer_matrices(idx):
+    c = workloads.LLAMA7B_LAYER
+    _, n_out, n_in = c["matrices"][idx]
+    w_base, w_ft = synth.matrix_pair(n_out, n_in, c["sigma"], c["b"], workloads.matrix_seed(c["seed"], idx), "cuda")
+    check_against_oracle(w_base, w_ft, c["mode"])
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA70B_PREFILL["matrices"])))
+def test_llama70b_matrices_per_row_alpha(idx):
+    c = workloads.LLAMA70B_PREFILL
+    _, n_out, n_in = c["matrices"][idx]
+    w_base, w_ft = synth.matrix_pair(n_out, n_in, c["sigma"], c["b"], workloads.matrix_seed(c["seed"], idx), "cuda")
+    check_against_oracle(w_base, w_ft, c["mode"])
+    # the same matrix with a scalar alpha as well
+    check_against_oracle(w_base, w_ft, 0)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_alpha_is_bitwise_reproducible(mode):
+    w_base, w_ft = synth.matrix_pair(4096, 11008, 0.02, 1e-3, seed=5, device="cuda")
+    b1, a1 = gpu_compress(w_base, w_ft, mode)
+    b2, a2 = gpu_compress(w_base, w_ft, mode)
+    assert torch.equal(b1, b2)
+    assert torch.equal(a1.view(torch.int32), a2.view(torch.int32))
+
+
+def test_zero_delta_packs_all_ones_and_alpha_zero():
+    w_base = synth.bf16_normal((64, 256), 0.02, synth.generator(1, "cuda"), "cuda")
+    bits, alpha = gpu_compress(w_base, w_base.clone(), 1)
+    assert torch.all(bits == 255)
+    assert torch.all(alpha == 0)

@@ -1,0 +1,175 @@
+"""GPU fused linear (bd_linear) against the fp64 oracle, through the C ABI.
+
+Both kernels are exercised: the HBM-streaming one (forced path 1, m <= 64) and
+the tcgen05 tensor-core one (forced path 2, any m), plus the automatic choice.
+Small cases compare every output; the full workload sizes compare sampled
+outputs that the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+from bit_delta_tenant_gb300 import bitdelta as bd
+from bit_delta_tenant_gb300 import synth, workloads
+from helpers import LinearCase, assert_y_close, sample_outputs, with_linear_path, y_host
+
+pytestmark = pytest.mark.gpu
+
+AUTO, STREAM, TENSOR = 0, 1, 2
+
+
+def full_check(case: LinearCase, path: int, what: str):
+    with with_linear_path(path):
+        y = case.run_linear()
+    torch.cuda.synchronize()
+    assert bd.bd_get_device_status() == bd.BD_OK
+    y_ref, mag = case.reference()
+    assert_y_close(y_host(y), y_ref, mag, what)
+
+
+def sampled_check(case: LinearCase, path: int, count: int, what: str):
+    with with_linear_path(path):
+        y = case.run_linear()
+    torch.cuda.synchronize()
+    assert bd.bd_get_device_status() == bd.BD_OK
+    yh = y_host(y)
+    assert np.all(np.isfinite(yh)), f"{what}: non-finite output"
+    ts, js = sample_outputs(case.m, case.n_out, count, seed=case.m + case.n_out)
+    y_ref, mag = case.reference_sampled(ts, js)
+    assert_y_close(yh[ts, js], y_ref, mag, what)
+
+
+@pytest.mark.parametrize("path", [AUTO, STREAM, TENSOR])
+def test_tiny_workload(path):
+    c = workloads.TINY
+    case = LinearCase(c["n_out"], c["n_in"], c["m"], c["sigma"], c["b"], c["mode"], c["seed"])
+    full_check(case, path, f"tiny path={path}")
+
+
+STREAM_SHAPES = [  # (n_out, n_in, m): ragged K (not multiples of 128), odd rows, every token-tile count
+    (1, 8, 1), (7, 16, 2), (129, 24, 3), (128, 120, 15), (33, 136, 16), (200, 4096, 17), (64, 1000, 33),
+    (130, 520, 64), (256, 4096, 8), (1, 11008, 4), (300, 264, 40),
+]
+
+
+@pytest.mark.parametrize("n_out,n_in,m", STREAM_SHAPES)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_streaming_kernel_shapes(n_out, n_in, m, mode):
+    case = LinearCase(n_out, n_in, m, 0.02, "row:5e-4:2e-3" if mode else 1e-3, mode, seed=n_out + 7 * n_in + m)
+    full_check(case, STREAM, f"stream {n_out}x{n_in} m={m}")
+
+
+TENSOR_SHAPES = [  # ragged in every dimension: rows vs 128, tokens vs 256, K vs 64
+    (128, 64, 256), (129, 64, 1), (7, 8, 5), (128, 72, 257), (300, 136, 100), (256, 1024, 511),
+    (200, 520, 512), (384, 4096, 513), (129, 24, 65), (64, 4104, 300),
+]
+
+
+@pytest.mark.parametrize("n_out,n_in,m", TENSOR_SHAPES)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tensor_core_kernel_shapes(n_out, n_in, m, mode):
+    case = LinearCase(n_out, n_in, m, 0.02, "row:5e-4:2e-3" if mode else 1e-3, mode, seed=3 * n_out + n_in + m)
+    full_check(case, TENSOR, f"tcgen05 {n_out}x{n_in} m={m}")
+
+
+@pytest.mark.parametrize("path", [STREAM, TENSOR])
+def test_alpha_zero_is_plain_base_linear(path):
+    case = LinearCase(96, 256, 16, seed=11)
+    case.alpha.zero_()
+    case.alpha32_h[:] = 0
+    full_check(case, path, "alpha=0")
+
+
+@pytest.mark.parametrize("path", [STREAM, TENSOR])
+def test_zero_base_unit_alpha_is_exact_sign_product(path):
+    """W_base = 0, alpha = 1, integer x: y = x . S^T exactly (|y| <= 8*n_in fits bf16 exactly here)."""
+    rng = np.random.default_rng(3)
+    n_out, n_in, m = 64, 32, 8
+    s = rng.choice(np.array([-1, 1]), size=(n_out, n_in))
+    xi = rng.integers(-2, 3, size=(m, n_in))
+    case = LinearCase(n_out, n_in, m, seed=1)
+    case.w_base.zero_()
+    case.wb_h[:] = 0
+    case.bits_h[:] = np.packbits(s > 0, axis=1, bitorder="little")
+    case.bits.copy_(torch.from_numpy(case.bits_h))
+    case.alpha.fill_(1.0)
+    case.alpha32_h[:] = 1.0
+    case.x.copy_(torch.from_numpy(xi.astype(np.float32)).to(torch.bfloat16))
+    case.x_h = synth.as_u16(case.x)
+    with with_linear_path(path):
+        y = case.run_linear()
+    torch.cuda.synchronize()
+    assert np.array_equal(y_host(y), (xi @ s.T).astype(np.float64))
+
+
+def test_empty_batch_is_a_no_op():
+    case = LinearCase(64, 128, 0, seed=2)
+    y = case.run_linear()
+    assert y.shape == (0, 64)
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA7B_LAYER["matrices"])))
+def test_llama7b_layer_decode_full_size(idx):
+    c = workloads.LLAMA7B_LAYER
+    name, n_out, n_in = c["matrices"][idx]
+    case = LinearCase(n_out, n_in, 1, c["sigma"], c["b"], c["mode"], workloads.matrix_seed(c["seed"], idx))
+    for m in c["ms"]:
+        case.set_m(m, seed=1000 + m)
+        sampled_check(case, AUTO, 1500, f"{name} m={m}")
+
+
+@pytest.mark.parametrize("idx", range(len(workloads.LLAMA70B_PREFILL["matrices"])))
+def test_llama70b_prefill_full_size(idx):
+    c = workloads.LLAMA70B_PREFILL
+    name, n_out, n_in = c["matrices"][idx]
+    case = LinearCase(n_out, n_in, 1, c["sigma"], c["b"], c["mode"], workloads.matrix_seed(c["seed"], idx))
+    for m in c["ms"]:
+        case.set_m(m, seed=2000 + m)
+        sampled_check(case, AUTO, 1500, f"{name} m={m}")
+    del case
+    torch.cuda.empty_cache()
+
+
+def test_both_kernels_agree_with_oracle_at_the_dispatch_boundary():
+    for m in (63, 64, 65):
+        case = LinearCase(512, 2048, m, seed=m)
+        y_ref, mag = case.reference()
+        for path in (STREAM, TENSOR) if m <= 64 else (TENSOR,):
+            with with_linear_path(path):
+                y = case.run_linear()
+            torch.cuda.synchronize()
+            assert_y_close(y_host(y), y_ref, mag, f"m={m} path={path}")
+
+
+def test_repeated_calls_on_a_side_stream():
+    case = LinearCase(256, 1024, 300, seed=4)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y1 = case.run_linear(s)
+        y2 = case.run_linear(s)
+    s.synchronize()
+    assert torch.equal(y1, y2)
+    y_ref, mag = case.reference()
+    assert_y_close(y_host(y1), y_ref, mag, "side stream")
+
+
+def test_wait_limit_zero_reports_timeout_and_context_survives():
+    """A zero wait limit makes the tensor-core kernel give up at its first
+    unsatisfied wait: it records a timeout, drains its own copies and returns.
+    The context stays usable and a normal call afterwards is correct."""
+    case = LinearCase(256, 4096, 512, seed=9)
+    assert bd.bd_get_device_status() == bd.BD_OK
+    prev = bd.bd_set_wait_limit_ns(0)
+    try:
+        with with_linear_path(TENSOR):
+            case.run_linear()
+        status = bd.bd_get_device_status()
+    finally:
+        bd.bd_set_wait_limit_ns(prev)
+    assert status == bd.BD_ERR_DEVICE_TIMEOUT
+    assert bd.bd_get_device_status() == bd.BD_OK      # read-and-clear
+    with with_linear_path(TENSOR):
+        y = case.run_linear()
+    torch.cuda.synchronize()
+    assert bd.bd_get_device_status() == bd.BD_OK
+    y_ref, mag = case.reference()
+    assert_y_close(y_host(y), y_ref, mag, "after timeout")
