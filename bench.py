@@ -1,0 +1,544 @@
+#!/usr/bin/env python3
+"""Benchmark of the BitDelta hot path on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+compression of every matrix of the workload (delta, sign packing, alpha) and
+the fused linear of every matrix at every token count of the workload; the
+multi-tenant workload adds the per-token-variant linear.  Inputs are resident
+in HBM when the timed region starts; each phase is captured once as a CUDA
+graph and replayed, so host launch overhead is not timed, and CUDA events on
+the replay stream bracket every phase (they give the per-kernel roofline).
+
+The default workload is the Llama-7B-style layer at decode sizes (q/k/v/o
+4096x4096, gate/up 11008x4096, down 4096x11008; m = 1, 4, 16).  Its inputs
+(about 1.2 GB of W_base + W_ft + packed bits) are larger than L2, and the step
+order separates the two uses of any matrix by more than 250 MB of other
+traffic, so kernels read from HBM.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle on
+the host cores (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from bit_delta_tenant_gb300 import synth, workloads  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# --------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    except Exception:
+        return dict(hbm=FALLBACK_HBM_GBS, bf16=FALLBACK_BF16_TFLOPS, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, value: float) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- workloads
+
+class Phase:
+    """A list of C-ABI calls replayed as one CUDA graph; algorithmic work per replay."""
+
+    def __init__(self, name, calls, bytes_=0.0, flops=0.0, launches=0, bound="hbm"):
+        self.name, self.calls, self.bytes, self.flops, self.launches, self.bound = \
+            name, calls, bytes_, flops, launches, bound
+        self.graph = None
+
+    def run(self):
+        for c in self.calls:
+            c()
+
+    def capture(self, stream):
+        self.run()                     # eager warm-up: sets kernel attributes, caches device info
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.run()
+        self.graph = g
+
+    def replay(self):
+        self.graph.replay()
+
+
+def compress_phase(bd, mats, mode, dev):
+    """bd_compress over every (W_base, W_ft) of `mats`; outputs kept for the linear phases."""
+    calls, nbytes = [], 0.0
+    outs = []
+    for (wb, wf) in mats:
+        n_out, n_in = wb.shape
+        bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=dev)
+        alpha = torch.empty((n_out if mode == 1 else 1,), dtype=torch.float32, device=dev)
+        ws = torch.empty((max(16, bd.bd_compress_workspace_size(n_out, n_in, mode)),), dtype=torch.uint8, device=dev)
+        calls.append(lambda wb=wb, wf=wf, bits=bits, alpha=alpha, ws=ws: bd.bd_compress(wb, wf, mode, bits, alpha, ws))
+        nbytes += 4.0 * n_out * n_in + n_out * n_in / 8 + 4.0 * (n_out if mode == 1 else 1)
+        outs.append((bits, alpha))
+    return Phase("compress", calls, bytes_=nbytes, launches=2 * len(mats)), outs
+
+
+def decode_bytes(m, n_out, n_in, mode):
+    return 2.0 * n_out * n_in + n_out * n_in / 8 + 4.0 * (n_out if mode == 1 else 1) + 2.0 * m * n_in + 2.0 * m * n_out
+
+
+class LayerDecode:
+    """Llama-7B-style layer linears at decode sizes (the default workload)."""
+    cfg = workloads.LLAMA7B_LAYER
+    metric_unit = "GB/s"
+
+    def __init__(self, bd, dev):
+        c = self.cfg
+        self.mats = [synth.matrix_pair(n_out, n_in, c["sigma"], c["b"], workloads.matrix_seed(c["seed"], i), dev)
+                     for i, (_, n_out, n_in) in enumerate(c["matrices"])]
+        self.comp, self.packed = compress_phase(bd, self.mats, c["mode"], dev)
+        self.xs, self.ys, calls, nbytes = {}, {}, [], 0.0
+        for m in c["ms"]:
+            for i, (name, n_out, n_in) in enumerate(c["matrices"]):
+                x = synth.activations(m, n_in, 10_000 + 97 * i + m, dev)
+                y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+                self.xs[(m, i)], self.ys[(m, i)] = x, y
+                wb = self.mats[i][0]
+                bits, alpha = self.packed[i]
+                calls.append(lambda x=x, wb=wb, bits=bits, alpha=alpha, y=y:
+                             bd.bd_linear(x, wb, bits, alpha, c["mode"], y))
+                nbytes += decode_bytes(m, n_out, n_in, c["mode"])
+        self.dec = Phase("decode", calls, bytes_=nbytes, launches=len(calls))
+        self.phases = [self.comp, self.dec]
+        self.dominant = self.dec
+        self.config = {"workload": c["name"], "matrices": [f"{n}:{a}x{b}" for n, a, b in c["matrices"]],
+                       "tokens": list(c["ms"]), "alpha": "scalar", "dtype_in": "bf16 weights/activations",
+                       "l2": "inputs larger than L2 (~1.2 GB touched per step; two uses of a matrix are "
+                             "separated by >250 MB of other traffic)"}
+
+    def step_bytes(self):
+        return sum(p.bytes for p in self.phases)
+
+    def e2e_buffers(self):
+        """Per-step host->device inputs (activations, fine-tuned weights) and device->host results."""
+        h2d = [(torch.empty_like(wf, device="cpu").pin_memory(), wf) for (_, wf) in self.mats]
+        h2d += [(torch.empty_like(x, device="cpu").pin_memory(), x) for x in self.xs.values()]
+        for host, devt in h2d:
+            host.copy_(devt)
+        d2h = [(torch.empty_like(y, device="cpu").pin_memory(), y) for y in self.ys.values()]
+        d2h += [(torch.empty_like(a, device="cpu").pin_memory(), a) for (_, a) in self.packed]
+        return h2d, d2h
+
+    def oracle_sample(self, oracle, frac_rows: float):
+        """Bounded CPU sample of one step: the first `frac_rows` of every matrix's rows."""
+        c = self.cfg
+        host = []
+        for i, (wb, wf) in enumerate(self.mats):
+            n = max(8, int(wb.shape[0] * frac_rows))
+            host.append((synth.as_u16(wb[:n]), synth.as_u16(wf[:n])))
+        xs = {k: synth.as_u16(v) for k, v in self.xs.items()}
+
+        def run():
+            nbytes = 0.0
+            packed = []
+            for (wb, wf) in host:
+                bits, a32, _ = oracle.compress(wb, wf, c["mode"])
+                packed.append((bits, a32))
+                nbytes += 4.0 * wb.size + wb.size / 8 + 4.0
+            for (m, i), x in xs.items():
+                wb = host[i][0]
+                bits, a32 = packed[i]
+                oracle.linear(x, wb, bits, a32, c["mode"])
+                nbytes += decode_bytes(m, wb.shape[0], wb.shape[1], c["mode"])
+            return nbytes
+        desc = f"every matrix's first {frac_rows:.4g} of rows: compress + fused linear at m=1,4,16"
+        return run, desc
+
+
+WORKLOADS = {"llama7b_layer_decode": LayerDecode}
+
+
+# --------------------------------------------------------------------------- arms
+
+def run_ours(args, ws, rank, local):
+    from bit_delta_tenant_gb300 import build as lib_build
+    if rank == 0:
+        lib_build.build()
+    barrier(ws)
+    from bit_delta_tenant_gb300 import bitdelta as bd
+    bd.load_library()
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    peaks = load_peaks()
+    wl = WORKLOADS[args.workload](bd, dev)
+    stream = torch.cuda.Stream(device=dev)
+    for p in wl.phases:
+        p.capture(stream)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for p in wl.phases:
+                p.replay()
+    torch.cuda.synchronize()
+    assert bd.bd_get_device_status() == bd.BD_OK
+
+    n_ev = len(wl.phases)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            for j, p in enumerate(wl.phases):
+                p.replay()
+                ev[k][j + 1].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clock_info = clocks.stop() if clocks else None
+    total_ms = start.elapsed_time(end)
+    phase_ms = [0.0] * n_ev
+    for k in range(args.steps):
+        for j in range(n_ev):
+            phase_ms[j] += ev[k][j].elapsed_time(ev[k][j + 1])
+    status = bd.bd_get_device_status()
+    if status != bd.BD_OK:
+        raise RuntimeError(f"device status after timing: {bd.bd_status_string(status)}")
+
+    t_max = max_over_ranks(ws, total_ms)
+    step_bytes = wl.step_bytes()
+    value = ws * args.steps * step_bytes / (t_max * 1e-3) / 1e9
+
+    dom = wl.dominant
+    dom_idx = wl.phases.index(dom)
+    dom_launch_s = phase_ms[dom_idx] * 1e-3 / (args.steps * dom.launches)
+    if dom.bound == "hbm":
+        achieved = dom.bytes / dom.launches / dom_launch_s / 1e9
+        peak, unit = peaks["hbm"], "GB/s"
+    else:
+        achieved = dom.flops / dom.launches / dom_launch_s / 1e12
+        peak, unit = peaks["bf16"], "TFLOP/s"
+    breakdown = {}
+    for j, p in enumerate(wl.phases):
+        t = phase_ms[j] * 1e-3 / args.steps
+        if p.bound == "hbm":
+            breakdown[p.name] = {"ms_per_step": t * 1e3, "GB/s": p.bytes / t / 1e9,
+                                 "frac_of_measured_hbm": p.bytes / t / 1e9 / peaks["hbm"],
+                                 "launches": p.launches}
+        else:
+            breakdown[p.name] = {"ms_per_step": t * 1e3, "TFLOP/s": p.flops / t / 1e12,
+                                 "frac_of_measured_bf16": p.flops / t / 1e12 / peaks["bf16"],
+                                 "launches": p.launches}
+
+    e2e = run_e2e(args, wl, stream, ws) if not args.no_e2e else None
+    cpu = cpu_baseline(wl, args) if (rank == 0 and not args.no_cpu) else None
+
+    line = {
+        "metric": "BitDelta fused linear GB/s (decode) & TFLOP/s (prefill), % of roofline",
+        "value": value, "unit": wl.metric_unit, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; N(0,sigma) bf16 base, Laplace deltas, N(0,1) activations)",
+        "config": dict(wl.config, parallelism=f"replicas{ws}" if ws > 1 else "single"),
+        "roofline": {"bound": dom.bound, "kernel": dom.name, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "peak_source": peaks["source"], "traffic": None},
+        "breakdown": breakdown,
+        "e2e": e2e,
+        "gpu_launches": args.steps * sum(p.launches for p in wl.phases),
+        "clocks": clock_info,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, wl, stream, ws):
+    """Same step through the C ABI with host buffers: H2D of the step's inputs, kernels, D2H of results."""
+    h2d, d2h = wl.e2e_buffers()
+    bi = sum(t.numel() * t.element_size() for t, _ in h2d)
+    bo = sum(t.numel() * t.element_size() for t, _ in d2h)
+
+    def one():
+        for host, devt in h2d:
+            devt.copy_(host, non_blocking=True)
+        for p in wl.phases:
+            p.replay()
+        for host, devt in d2h:
+            host.copy_(devt, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            one()
+    torch.cuda.synchronize()
+    barrier(ws)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for _ in range(args.steps):
+            one()
+        e.record(stream)
+    torch.cuda.synchronize()
+    t = max_over_ranks(ws, s.elapsed_time(e))
+    return {"value": ws * args.steps * wl.step_bytes() / (t * 1e-3) / 1e9, "unit": wl.metric_unit,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": t / args.steps}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, args, target_s: float = 12.0):
+    import oracle
+    oracle.build()
+    frac = 1.0 / 64
+    run, _ = wl.oracle_sample(oracle, frac)
+    t0 = time.perf_counter()
+    run()
+    t1 = time.perf_counter() - t0
+    frac = min(1.0, frac * max(1.0, target_s / max(t1, 1e-3)))
+    run, desc = wl.oracle_sample(oracle, frac)
+    t0 = time.perf_counter()
+    nbytes = run()
+    dt = time.perf_counter() - t0
+    return {"value": nbytes / dt / 1e9, "unit": wl.metric_unit, "cores": cpu_cores(), "kind": "oracle",
+            "sample": desc, "seconds": dt}
+
+
+def run_reference(args, ws, rank):
+    """The fp64 CPU oracle as it stands, on the host cores; rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    from bit_delta_tenant_gb300 import bitdelta as bd  # noqa: F401  (workload construction only)
+    wl = WORKLOADS[args.workload](_NoLib(), dev)
+    frac = 1.0 / 16
+    run, desc = wl.oracle_sample(oracle, frac)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for _ in range(args.steps):
+        nbytes = run()
+    dt = time.perf_counter() - t0
+    v = args.steps * nbytes / dt / 1e9
+    line = {"impl": "reference", "metric": "BitDelta fused linear GB/s (decode) & TFLOP/s (prefill), % of roofline",
+            "value": v, "unit": wl.metric_unit, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": wl.config,
+            "cpu_baseline": {"value": v, "unit": wl.metric_unit, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": v, "unit": wl.metric_unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+class _NoLib:
+    """Stands in for the library when only the workload's inputs are needed (reference arm)."""
+
+    def bd_compress_workspace_size(self, *a):
+        return 16
+
+    def __getattr__(self, name):
+        def _never(*a, **k):
+            raise RuntimeError("the reference arm does not call the GPU library")
+        return _never
+
+
+def run_kernel_case(args):
+    """One kernel on one shape, launched eagerly (no graph): for ncu captures and sweeps.
+
+    --kernel-case linear:N_OUTxN_IN:M[:path]  or  compress:N_OUTxN_IN[:mode]
+    Rotates over enough copies of the weights that the working set exceeds L2.
+    """
+    from bit_delta_tenant_gb300 import build as lib_build
+    lib_build.build()
+    from bit_delta_tenant_gb300 import bitdelta as bd
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    parts = args.kernel_case.split(":")
+    kind, shape = parts[0], parts[1]
+    n_out, n_in = (int(v) for v in shape.split("x"))
+    per = 2.0 * n_out * n_in
+    copies = max(1, int(np.ceil(3 * 129e6 / per)))
+    mats = [synth.matrix_pair(n_out, n_in, 0.02, 1e-3, 50 + i, dev) for i in range(copies)]
+    if kind == "linear":
+        m = int(parts[2])
+        path = int(parts[3]) if len(parts) > 3 else 0
+        bd.bd_set_linear_path(path)
+        packed = []
+        for wb, wf in mats:
+            bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=dev)
+            alpha = torch.empty((1,), dtype=torch.float32, device=dev)
+            ws = torch.empty((max(16, bd.bd_compress_workspace_size(n_out, n_in, 0)),), dtype=torch.uint8,
+                             device=dev)
+            bd.bd_compress(wb, wf, 0, bits, alpha, ws)
+            packed.append((bits, alpha))
+        x = synth.activations(m, n_in, 7, dev)
+        y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+
+        def call(i):
+            bd.bd_linear(x, mats[i][0], packed[i][0], packed[i][1], 0, y)
+        work = decode_bytes(m, n_out, n_in, 0)
+        flops = 2.0 * m * n_out * n_in
+    else:
+        mode = int(parts[2]) if len(parts) > 2 else 0
+        bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=dev)
+        alpha = torch.empty((n_out if mode else 1,), dtype=torch.float32, device=dev)
+        ws = torch.empty((max(16, bd.bd_compress_workspace_size(n_out, n_in, mode)),), dtype=torch.uint8,
+                         device=dev)
+
+        def call(i):
+            bd.bd_compress(mats[i][0], mats[i][1], mode, bits, alpha, ws)
+        work = 4.0 * n_out * n_in + n_out * n_in / 8
+        flops = 0.0
+    for i in range(args.warmup):
+        call(i % copies)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for k in range(args.steps):
+        evs[k][0].record()
+        call(k % copies)
+        evs[k][1].record()
+    torch.cuda.synchronize()
+    times = sorted(a.elapsed_time(b) for a, b in evs)
+    med = times[len(times) // 2] * 1e-3
+    assert bd.bd_get_device_status() == bd.BD_OK
+    print(json.dumps({"kernel_case": args.kernel_case, "copies": copies, "median_us": med * 1e6,
+                      "GB/s": work / med / 1e9, "TFLOP/s": flops / med / 1e12}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama7b_layer_decode")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--kernel-case", default=None,
+                    help="linear:N_OUTxN_IN:M[:path] or compress:N_OUTxN_IN[:mode] (one kernel, eager)")
+    args = ap.parse_args()
+    if args.kernel_case:
+        run_kernel_case(args)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup() if args.impl == "ours" else (int(os.environ.get("WORLD_SIZE", "1")),
+                                                                 int(os.environ.get("RANK", "0")), 0)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
