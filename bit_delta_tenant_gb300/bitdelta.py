@@ -28,6 +28,7 @@ BD_ERR_BAD_VARIANT_ID = 7
 BD_ALPHA_SCALAR = 0
 BD_ALPHA_PER_ROW = 1
 BD_MAX_VARIANTS = 64
+BD_NOALLOC_MAX_PARTIALS = 131072
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +65,8 @@ def load_library(path: str | None = None):
         lib.bd_compress_workspace_size.restype = SZ
         lib.bd_compress.argtypes = [V, V, I64, I64, I32, V, V, V, SZ, V]
         lib.bd_compress.restype = I32
+        lib.bd_compress_noalloc.argtypes = [V, V, I64, I64, I32, V, V, V]
+        lib.bd_compress_noalloc.restype = I32
         lib.bd_linear.argtypes = [V, I64, V, V, V, I32, I64, I64, V, V]
         lib.bd_linear.restype = I32
         lib.bd_linear_grouped_workspace_size.argtypes = [I64, I32, I64, I64]
@@ -124,6 +127,20 @@ def bd_compress(w_base: torch.Tensor, w_ft: torch.Tensor, alpha_mode: int, bits_
                                     _ptr(alpha_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream))
     _check(rc, "bd_compress")
+
+
+def bd_compress_noalloc(w_base: torch.Tensor, w_ft: torch.Tensor, alpha_mode: int, bits_out: torch.Tensor,
+                        alpha_out: torch.Tensor, stream=None) -> None:
+    """bd_compress without a workspace, for callers that cannot allocate device memory.
+
+    Uses the library's built-in 1 MiB scratch array; shapes needing more partial
+    sums than BD_NOALLOC_MAX_PARTIALS raise (status BD_ERR_WORKSPACE).  Calls
+    that overlap on the GPU share that array and race: keep them ordered.
+    """
+    n_out, n_in = w_base.shape
+    rc = load_library().bd_compress_noalloc(_ptr(w_base), _ptr(w_ft), n_out, n_in, int(alpha_mode),
+                                            _ptr(bits_out), _ptr(alpha_out), _stream(stream))
+    _check(rc, "bd_compress_noalloc")
 
 
 def bd_linear(x: torch.Tensor, w_base: torch.Tensor, bits: torch.Tensor, alpha: torch.Tensor, alpha_mode: int,

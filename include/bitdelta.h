@@ -99,6 +99,36 @@ int32_t bd_compress(const void *w_base, const void *w_ft, int64_t n_out,
                     void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * Compression without a workspace.  The page has no counterpart to this
+ * entry point; it exists for callers that cannot hand the library any device
+ * memory besides the inputs and outputs -- for example code running under a
+ * framework that owns all device memory through a pre-planned arena, or a
+ * latency-critical path that must not call cudaMalloc (which can
+ * synchronise the device).
+ *
+ * Same arguments, results and errors as bd_compress, minus the workspace:
+ * the partial sums live in a fixed scratch array built into the library,
+ * BD_NOALLOC_MAX_PARTIALS doubles (1 MiB) per GPU that loads the library,
+ * held until the process exits.  A shape fits when
+ *   rows * ceil(chunks / 2048) <= BD_NOALLOC_MAX_PARTIALS,
+ * with rows = 1 and chunks = n_out*n_in/8 for a scalar alpha (up to 2^31
+ * elements), or rows = n_out and chunks = n_in/8 per row; larger shapes
+ * return BD_ERR_WORKSPACE before launching anything (use bd_compress).
+ * The call allocates and frees nothing.  Its first call on a device looks
+ * up the scratch array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All
+ * calls in the process share the one array, and every slot a call reads is
+ * written earlier by the same call, so stale contents never matter -- but
+ * calls whose kernels overlap on the GPU (different streams without
+ * ordering) race on it: order them on one stream or with events.
+ * ------------------------------------------------------------------------ */
+#define BD_NOALLOC_MAX_PARTIALS 131072
+
+int32_t bd_compress_noalloc(const void *w_base, const void *w_ft,
+                            int64_t n_out, int64_t n_in, int32_t alpha_mode,
+                            uint8_t *bits_out, float *alpha_out, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Fused linear  ([serve] fused reconstruction + matmul, never materialising
  * W_eff in HBM; the conceptual fused_bitdelta_linear listing)
  *
