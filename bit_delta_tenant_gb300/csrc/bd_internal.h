@@ -54,12 +54,27 @@ cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const u
                            cudaStream_t stream);
 
 // ---- multi-tenant ----------------------------------------------------------------------
+constexpr int kMaxVariantsDev = 64;  // = BD_MAX_VARIANTS
 struct GroupedVariants {
-    const uint8_t *bits[64];
-    const float *alpha[64];
-    int32_t mode[64];
+    const uint8_t *bits[kMaxVariantsDev];
+    const float *alpha[kMaxVariantsDev];
+    int32_t mode[kMaxVariantsDev];
     int32_t count;
 };
+// Device-built schedule of the multi-tenant tensor-core path: `tiles` holds
+// (variant, first row in the variant-sorted activations, rows <= 256) per
+// token tile, `*n_tiles` how many are valid, `perm` maps sorted rows back to
+// original tokens; the grid is sized for `max_slots` tiles per W row tile.
+struct GroupTable {
+    const int32_t *tiles;
+    const int32_t *n_tiles;
+    const int32_t *perm;
+    int32_t max_slots;
+};
+cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
+                                   int64_t n_out, int64_t n_in, void *y, const GroupTable &tab, const DevCtx &ctx,
+                                   cudaStream_t stream);
+
 size_t grouped_workspace_size(int64_t m, int32_t n_variants, int64_t n_out, int64_t n_in);
 cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const void *w_base,
                            const GroupedVariants &vars, int64_t n_out, int64_t n_in, void *y, void *ws,

@@ -42,6 +42,7 @@ constexpr uint32_t kStageTx = kWBytes + kXBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 256;
 constexpr size_t kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 256;
+constexpr int kMaxVariants = 64;
 
 struct PrefillArgs {
     const uint8_t *bits;
@@ -54,6 +55,16 @@ struct PrefillArgs {
     int32_t bits_vec8;  // rows of packed bits are 8-byte aligned
     unsigned *status;
     uint64_t wait_ns;
+    // Multi-tenant mode only: token tiles come from a device-built table of
+    // (variant, first row in the variant-sorted activations, row count), and
+    // output rows are scattered back to the original token order through perm.
+    const int32_t *tiles;
+    const int32_t *n_tiles;
+    const int32_t *perm;
+    int32_t max_slots;
+    const uint8_t *vbits[kMaxVariants];
+    const float *valpha[kMaxVariants];
+    int32_t vmode[kMaxVariants];
 };
 
 __device__ __forceinline__ uint32_t rebuild_pair(uint32_t w, uint32_t byte, int i, float al) {
@@ -67,9 +78,10 @@ __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *stat
     flag_status(status, kDevTimeout);
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                   PrefillArgs a) {
+                   const __grid_constant__ PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;
@@ -82,17 +94,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    // Grouped rasterisation: consecutive CTAs cycle over `group` token tiles
-    // for one W tile, so a wave touches a compact block of W and x in L2.
-    const int tile = blockIdx.x;
-    const int per_group = a.group * a.row_tiles;
-    const int grp = tile / per_group;
-    const int rem = tile - grp * per_group;
-    const int gsize = min(a.group, a.tok_tiles - grp * a.group);
-    const int tok_tile = grp * a.group + rem % gsize;
-    const int row_tile = rem / gsize;
-    const int m0 = row_tile * kBM;
-    const int n0 = tok_tile * kBN;
+    int m0, n0, count;
+    const uint8_t *bits;
+    const float *alpha;
+    int32_t mode;
+    if constexpr (kGrouped) {
+        // Consecutive CTAs take every token tile of one W row tile, so the W
+        // tile is read from HBM once per wave and reused from L2.
+        const int row_tile = blockIdx.x / a.max_slots;
+        const int slot = blockIdx.x - row_tile * a.max_slots;
+        if (slot >= *a.n_tiles) return;  // uniform across the CTA, before any barrier or TMEM use
+        const int v = a.tiles[3 * slot];
+        m0 = row_tile * kBM;
+        n0 = a.tiles[3 * slot + 1];
+        count = a.tiles[3 * slot + 2];
+        bits = a.vbits[v];
+        alpha = a.valpha[v];
+        mode = a.vmode[v];
+    } else {
+        // Grouped rasterisation: consecutive CTAs cycle over `group` token tiles
+        // for one W tile, so a wave touches a compact block of W and x in L2.
+        const int tile = blockIdx.x;
+        const int per_group = a.group * a.row_tiles;
+        const int grp = tile / per_group;
+        const int rem = tile - grp * per_group;
+        const int gsize = min(a.group, a.tok_tiles - grp * a.group);
+        const int tok_tile = grp * a.group + rem % gsize;
+        const int row_tile = rem / gsize;
+        m0 = row_tile * kBM;
+        n0 = tok_tile * kBN;
+        count = static_cast<int>(min(static_cast<int64_t>(kBN), a.m - n0));
+        bits = a.bits;
+        alpha = a.alpha;
+        mode = a.mode;
+    }
+    // MMA N: the tile's token count rounded up to the 16-column granule of M=128.
+    const int n_mma = (count + 15) & ~15;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -142,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+            const uint32_t idesc = idesc_bf16_f32(kBM, n_mma);
             bool ok = true;
             for (int kb = 0; kb < nkb; ++kb) {
                 const int s = kb % kStages;
@@ -174,9 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = sub * 32 + lane;
         const int64_t row = static_cast<int64_t>(m0) + r;
         const bool row_ok = row < a.n_out;
-        const float al = row_ok ? (a.mode ? a.alpha[row] : a.alpha[0]) : 0.0f;
+        const float al = row_ok ? (mode ? alpha[row] : alpha[0]) : 0.0f;
         const int64_t bpr = a.n_in / 8;
-        const uint8_t *brow = a.bits + (row_ok ? row : 0) * bpr;
+        const uint8_t *brow = bits + (row_ok ? row : 0) * bpr;
 
         auto load_bits = [&](int kb) -> uint2 {
             uint2 v = make_uint2(0u, 0u);
@@ -239,15 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t *ycol = a.y + row;
 #pragma unroll 1
                 for (int c0 = 0; c0 < kBN; c0 += 32) {
-                    if (n0 + c0 >= a.m) break;  // warp-uniform
+                    if (c0 >= count) break;  // warp-uniform
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(lane_addr + c0, v);
                     tmem_ld_wait();
                     if (row_ok) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const int64_t t = static_cast<int64_t>(n0) + c0 + i;
-                            if (t < a.m) {
+                            if (c0 + i < count) {
+                                const int64_t t = kGrouped ? static_cast<int64_t>(a.perm[n0 + c0 + i])
+                                                           : static_cast<int64_t>(n0) + c0 + i;
                                 __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[i]));
                                 ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&h);
                             }
@@ -268,41 +306,86 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
-                           int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
-                           cudaStream_t stream) {
+namespace {
+
+template <bool kGrouped>
+cudaError_t set_smem_attr(const DevCtx &ctx) {
     static bool attr_set[128] = {false};
     if (ctx.device < 128 && !attr_set[ctx.device]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
-    CUtensorMap tm_w, tm_x;
-    if (!encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kBK, kBM,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    if (!encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, m, n_in * 2, kBK, kBN,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    PrefillArgs a;
-    a.bits = bits;
-    a.alpha = alpha;
+    return cudaSuccess;
+}
+
+void fill_common(PrefillArgs &a, int64_t m, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx) {
     a.y = static_cast<uint16_t *>(y);
     a.m = m;
     a.n_out = n_out;
     a.n_in = n_in;
-    a.mode = alpha_mode;
     a.num_kb = static_cast<int32_t>((n_in + kBK - 1) / kBK);
     a.row_tiles = static_cast<int32_t>((n_out + kBM - 1) / kBM);
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
+}
+
+bool make_maps(CUtensorMap &tm_w, CUtensorMap &tm_x, const void *w_base, const void *x, int64_t x_rows,
+               int64_t n_out, int64_t n_in) {
+    return encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kBK, kBM,
+                                CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, x_rows, n_in * 2, kBK, kBN,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                           int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                           cudaStream_t stream) {
+    cudaError_t e = set_smem_attr<false>(ctx);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm_w, tm_x;
+    if (!make_maps(tm_w, tm_x, w_base, x, m, n_out, n_in)) return cudaErrorInvalidValue;
+    PrefillArgs a = {};
+    fill_common(a, m, n_out, n_in, y, ctx);
+    a.bits = bits;
+    a.alpha = alpha;
+    a.mode = alpha_mode;
     a.tok_tiles = static_cast<int32_t>((m + kBN - 1) / kBN);
     a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
     a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
-    a.status = ctx.status;
-    a.wait_ns = ctx.wait_ns;
     const int64_t tiles = static_cast<int64_t>(a.row_tiles) * a.tok_tiles;
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    prefill_kernel<<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+    prefill_kernel<false><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
+                                   int64_t n_out, int64_t n_in, void *y, const GroupTable &tab, const DevCtx &ctx,
+                                   cudaStream_t stream) {
+    cudaError_t e = set_smem_attr<true>(ctx);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm_w, tm_x;
+    if (!make_maps(tm_w, tm_x, w_base, x_sorted, m, n_out, n_in)) return cudaErrorInvalidValue;
+    PrefillArgs a = {};
+    fill_common(a, m, n_out, n_in, y, ctx);
+    bool vec8 = (n_in / 8) % 8 == 0;
+    for (int v = 0; v < vars.count; ++v) {
+        a.vbits[v] = vars.bits[v];
+        a.valpha[v] = vars.alpha[v];
+        a.vmode[v] = vars.mode[v];
+        vec8 = vec8 && (reinterpret_cast<uintptr_t>(vars.bits[v]) & 7) == 0;
+    }
+    a.bits_vec8 = vec8 ? 1 : 0;
+    a.tiles = tab.tiles;
+    a.n_tiles = tab.n_tiles;
+    a.perm = tab.perm;
+    a.max_slots = tab.max_slots;
+    const int64_t grid = static_cast<int64_t>(a.row_tiles) * tab.max_slots;
+    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    prefill_kernel<true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
     return cudaGetLastError();
 }
 
