@@ -137,7 +137,7 @@ BD_API int64_t bd_set_wait_limit_ns(int64_t limit_ns) {
 
 BD_API int32_t bd_set_linear_path(int32_t path) {
     const int32_t prev = g_linear_path.load();
-    if (path >= 0 && path <= 2) g_linear_path.store(path);
+    if (path >= 0 && path <= 3) g_linear_path.store(path);
     return prev;
 }
 
@@ -204,14 +204,20 @@ BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uin
     if (rc != BD_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int32_t path = g_linear_path.load();
-    const bool decode_ok = bd::decode_supported(m, n_out, n_in, ctx.num_sms);
+    const bool tma_ok = bd::decode_tma_supported(m, n_out, n_in, w_base, bits, ctx.num_sms);
+    const bool decode_ok = tma_ok || bd::decode_supported(m, n_out, n_in, ctx.num_sms);
     bool use_decode = decode_ok && m <= bd::kDecodeMaxM;
     if (path == 1) {
         if (!decode_ok) return BD_ERR_UNSUPPORTED_SHAPE;
         use_decode = true;
     } else if (path == 2) {
         use_decode = false;
+    } else if (path == 3) {
+        if (!bd::decode_supported(m, n_out, n_in, ctx.num_sms)) return BD_ERR_UNSUPPORTED_SHAPE;
+        use_decode = true;
     }
+    if (use_decode && tma_ok && path != 3)
+        return cuda_status(bd::launch_decode_tma(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));
     if (use_decode)
         return cuda_status(bd::launch_decode(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));
     return cuda_status(bd::launch_prefill(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));

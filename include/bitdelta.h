@@ -208,8 +208,9 @@ int64_t bd_set_wait_limit_ns(int64_t limit_ns);
  * 0 = automatic (the HBM-streaming kernel for m <= 64 when its activation
  * slice fits in shared memory, the tensor-core kernel otherwise); 1 = always
  * the streaming kernel (BD_ERR_UNSUPPORTED_SHAPE where it cannot run);
- * 2 = always the tensor-core kernel.  Other values are ignored.  Returns the
- * previous value. */
+ * 2 = always the tensor-core kernel; 3 = always the register-fed streaming
+ * kernel (the fallback of 1 for n_in not a multiple of 128).  Other values
+ * are ignored.  Returns the previous value. */
 int32_t bd_set_linear_path(int32_t path);
 
 /* Library version, major * 10000 + minor * 100 + patch. */

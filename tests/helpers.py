@@ -88,7 +88,7 @@ def sample_outputs(m: int, n_out: int, count: int, seed: int = 0):
 
 
 def with_linear_path(path: int):
-    """Context manager forcing bd_linear's kernel choice (0 auto, 1 streaming, 2 tensor core)."""
+    """Context manager forcing bd_linear's kernel choice (0 auto, 1 streaming, 2 tensor core, 3 register-fed streaming)."""
     class _Ctx:
         def __enter__(self):
             self.prev = bd.bd_set_linear_path(path)

@@ -14,7 +14,7 @@ from helpers import LinearCase, assert_y_close, sample_outputs, with_linear_path
 
 pytestmark = pytest.mark.gpu
 
-AUTO, STREAM, TENSOR = 0, 1, 2
+AUTO, STREAM, TENSOR, STREAM_REG = 0, 1, 2, 3
 
 
 def full_check(case: LinearCase, path: int, what: str):
@@ -49,13 +49,18 @@ STREAM_SHAPES = [  # (n_out, n_in, m): ragged K (not multiples of 128), odd rows
     (1, 8, 1), (7, 16, 2), (129, 24, 3), (128, 120, 15), (33, 136, 16), (200, 4096, 17), (64, 1000, 33),
     (130, 520, 64), (256, 4096, 8), (1, 11008, 4), (300, 264, 40),
 ]
+TMA_STREAM_SHAPES = [  # n_in multiples of 128 (TMA-fed variant): ragged rows, slices, tokens
+    (64, 128, 1), (65, 256, 9), (300, 384, 33), (129, 1152, 64), (7, 2048, 16), (1000, 8192, 2),
+    (4096, 4096, 16), (63, 16384, 5), (2000, 640, 24),
+]
 
 
-@pytest.mark.parametrize("n_out,n_in,m", STREAM_SHAPES)
+@pytest.mark.parametrize("n_out,n_in,m", STREAM_SHAPES + TMA_STREAM_SHAPES)
 @pytest.mark.parametrize("mode", [0, 1])
-def test_streaming_kernel_shapes(n_out, n_in, m, mode):
+@pytest.mark.parametrize("path", [STREAM, STREAM_REG])
+def test_streaming_kernel_shapes(n_out, n_in, m, mode, path):
     case = LinearCase(n_out, n_in, m, 0.02, "row:5e-4:2e-3" if mode else 1e-3, mode, seed=n_out + 7 * n_in + m)
-    full_check(case, STREAM, f"stream {n_out}x{n_in} m={m}")
+    full_check(case, path, f"stream path={path} {n_out}x{n_in} m={m}")
 
 
 TENSOR_SHAPES = [  # ragged in every dimension: rows vs 128, tokens vs 256, K vs 64
@@ -71,7 +76,7 @@ def test_tensor_core_kernel_shapes(n_out, n_in, m, mode):
     full_check(case, TENSOR, f"tcgen05 {n_out}x{n_in} m={m}")
 
 
-@pytest.mark.parametrize("path", [STREAM, TENSOR])
+@pytest.mark.parametrize("path", [STREAM, STREAM_REG, TENSOR])
 def test_alpha_zero_is_plain_base_linear(path):
     case = LinearCase(96, 256, 16, seed=11)
     case.alpha.zero_()
@@ -79,11 +84,12 @@ def test_alpha_zero_is_plain_base_linear(path):
     full_check(case, path, "alpha=0")
 
 
-@pytest.mark.parametrize("path", [STREAM, TENSOR])
-def test_zero_base_unit_alpha_is_exact_sign_product(path):
-    """W_base = 0, alpha = 1, integer x: y = x . S^T exactly (|y| <= 8*n_in fits bf16 exactly here)."""
+@pytest.mark.parametrize("path", [STREAM, STREAM_REG, TENSOR])
+@pytest.mark.parametrize("n_in", [32, 128])
+def test_zero_base_unit_alpha_is_exact_sign_product(path, n_in):
+    """W_base = 0, alpha = 1, integer x: y = x . S^T exactly (|y| <= 2*n_in fits bf16 exactly here)."""
     rng = np.random.default_rng(3)
-    n_out, n_in, m = 64, 32, 8
+    n_out, m = 64, 8
     s = rng.choice(np.array([-1, 1]), size=(n_out, n_in))
     xi = rng.integers(-2, 3, size=(m, n_in))
     case = LinearCase(n_out, n_in, m, seed=1)
@@ -133,7 +139,7 @@ def test_both_kernels_agree_with_oracle_at_the_dispatch_boundary():
     for m in (63, 64, 65):
         case = LinearCase(512, 2048, m, seed=m)
         y_ref, mag = case.reference()
-        for path in (STREAM, TENSOR) if m <= 64 else (TENSOR,):
+        for path in (STREAM, STREAM_REG, TENSOR) if m <= 64 else (TENSOR,):
             with with_linear_path(path):
                 y = case.run_linear()
             torch.cuda.synchronize()
