@@ -80,6 +80,8 @@ int32_t check_matrix_shape(int64_t n_out, int64_t n_in) {
 
 namespace bd {
 
+int32_t make_dev_ctx(DevCtx *ctx) { return make_ctx(ctx); }
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

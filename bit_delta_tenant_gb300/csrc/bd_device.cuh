@@ -98,6 +98,23 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to shared memory, completion signalled on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// prologue, then wait until every kernel this one depends on has completed
+// and its writes are visible.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_trigger_and_wait() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Make this thread's generic-proxy writes to shared memory visible to the
 // async proxy (tensor core / TMA reads that are ordered after a barrier).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -23,6 +23,10 @@ struct DevCtx {
     int device;           // current device ordinal
 };
 
+// Device context of the current device (status word address, SM count, the
+// process-wide wait limit); returns a bd_status code.
+int32_t make_dev_ctx(DevCtx *ctx);
+
 // ---- compression -------------------------------------------------------------------
 constexpr int kCompressThreads = 256;
 constexpr int kCompressChunksPerThread = 8;                                        // 16-byte chunks

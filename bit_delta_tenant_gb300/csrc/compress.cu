@@ -13,14 +13,15 @@
 // least significant bit first; bit = 1 iff Delta >= 0 (zero of either sign
 // packs as 1).  Delta is formed in fp32 from the bf16 inputs.
 //
-// Data path: every thread owns 16-byte chunks (8 bf16) of both inputs, so one
-// chunk yields exactly one output byte in registers, with no cross-lane
-// exchange; lanes of a warp own consecutive chunks, so the loads are 512-byte
-// coalesced and the byte stores 32-byte coalesced.  |Delta| of a chunk is
-// summed pairwise in fp32 (8 terms), widened to fp64, reduced through the warp
-// with xor-shuffles and across warps in shared memory in a fixed order; each
-// block writes one fp64 partial.  A second kernel adds each row's partials in
-// a fixed order and rounds alpha to fp32 once, so alpha is bitwise
+// Data path: a persistent pass (two CTAs per SM) streams W_base and W_ft
+// through a shared-memory ring with 1-D bulk copies; every consumer thread
+// owns 16-byte chunks (8 bf16) of both inputs, so one chunk yields exactly one
+// output byte in registers with no cross-lane exchange, and lanes own
+// consecutive chunks, so the byte stores are 32-byte coalesced.  |Delta| is
+// summed pairwise in fp32 per thread (64 terms), widened to fp64, reduced
+// through the warp with xor-shuffles and across warps in a fixed order: one
+// fp64 partial per 2048-chunk segment.  A second kernel adds each row's
+// partials in a fixed order and rounds alpha to fp32 once, so alpha is bitwise
 // reproducible for a given shape on any device.
 #include "bd_device.cuh"
 #include "bd_internal.h"
@@ -37,8 +38,9 @@ struct CompressArgs {
     int64_t segs;
 };
 
-// Signs and |Delta| of one chunk: returns the packed byte, adds sum|Delta| to acc.
-__device__ __forceinline__ uint32_t chunk_signs(const uint4 &b, const uint4 &f, double &acc) {
+// Signs and |Delta| of one chunk: returns the packed byte and the pairwise
+// fp32 sum of the chunk's eight |Delta|.
+__device__ __forceinline__ uint32_t chunk_signs(const uint4 &b, const uint4 &f, float &sum) {
     const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
     const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
     float ad[8];
@@ -52,51 +54,139 @@ __device__ __forceinline__ uint32_t chunk_signs(const uint4 &b, const uint4 &f, 
         ad[2 * i] = fabsf(d_lo);
         ad[2 * i + 1] = fabsf(d_hi);
     }
-    const float s = ((ad[0] + ad[1]) + (ad[2] + ad[3])) + ((ad[4] + ad[5]) + (ad[6] + ad[7]));
-    acc += static_cast<double>(s);
+    sum = ((ad[0] + ad[1]) + (ad[2] + ad[3])) + ((ad[4] + ad[5]) + (ad[6] + ad[7]));
     return byte;
 }
 
-__global__ void __launch_bounds__(kCompressThreads) compress_pass1(CompressArgs a) {
-    const int64_t seg_id = blockIdx.x;
-    const int64_t row = seg_id / a.segs;
-    const int64_t seg = seg_id - row * a.segs;
-    const int64_t first = seg * kCompressChunksPerSeg;
-    const int64_t base = row * a.row_chunks;
-    const int tid = threadIdx.x;
+// Pass 1, persistent: CTA b walks segments b, b+G, b+2G, ... (2 CTAs per SM).
+// A producer warp streams each segment's W_base and W_ft bytes, half a
+// segment (1024 chunks, 32 KB) per ring slot, into a 3-slot shared-memory
+// ring with 1-D bulk copies; 256 consumer threads take chunk tid + 256u
+// (u = 0..7) of the segment.  A thread's eight chunk sums (fp32, pairwise over
+// 8 elements) are added pairwise in fp32, widened to fp64 and reduced with
+// xor-shuffles and across warps in a fixed order.  The assignment and order do
+// not depend on the grid, so each segment's partial (and alpha) is the same on
+// any device.  Worst-case relative error of a thread's fp32 sum: 6 levels of
+// pairwise rounding plus the fp32 subtraction, ~7 * 2^-24 < 5e-7.
+constexpr int kRingStages = 3;
+constexpr int kHalfChunks = kCompressChunksPerSeg / 2;
+constexpr uint32_t kHalfBytes = static_cast<uint32_t>(kHalfChunks) * 16;  // per tensor
+constexpr int kPass1Threads = kCompressThreads + 32;
+constexpr size_t kPass1Smem = 128 + kRingStages * 2 * kHalfBytes + 256;
 
-    uint4 vb[kCompressChunksPerThread], vf[kCompressChunksPerThread];
-#pragma unroll
-    for (int u = 0; u < kCompressChunksPerThread; ++u) {
-        const int64_t c = first + u * kCompressThreads + tid;
-        if (c < a.row_chunks) {
-            vb[u] = ldg_stream(a.wb + base + c);
-            vf[u] = ldg_stream(a.wf + base + c);
-        } else {
-            vb[u] = make_uint4(0, 0, 0, 0);
-            vf[u] = make_uint4(0, 0, 0, 0);
-        }
-    }
-    double acc = 0.0;
-#pragma unroll
-    for (int u = 0; u < kCompressChunksPerThread; ++u) {
-        const int64_t c = first + u * kCompressThreads + tid;
-        if (c < a.row_chunks) {
-            const uint32_t byte = chunk_signs(vb[u], vf[u], acc);
-            a.bits[base + c] = static_cast<uint8_t>(byte);
-        }
-    }
-    // Fixed-order fp64 reduction: xor-butterfly in the warp, then warps in order.
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    __shared__ double warp_sum[kCompressThreads / 32];
-    if ((tid & 31) == 0) warp_sum[tid >> 5] = acc;
-    __syncthreads();
+__global__ void __launch_bounds__(kPass1Threads, 2)
+    compress_pass1(const __grid_constant__ CompressArgs a, int64_t n_segs_total, unsigned *status,
+                   uint64_t wait_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kRingStages * 2 * kHalfBytes);
+    uint64_t *empty = full + kRingStages;
+    double *warp_sum = reinterpret_cast<double *>(empty + kRingStages);  // [2][8]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(warp_sum + 16);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     if (tid == 0) {
-        double s = 0.0;
+        for (int s = 0; s < kRingStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCompressThreads / 32);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_trigger_and_wait();
+
+    const int64_t first_seg = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    if (warp == kCompressThreads / 32) {
+        if (lane == 0) {
+            int j = 0, issued = 0;
+            bool stop = false;
+            for (int64_t sg = first_seg; sg < n_segs_total && !stop; sg += stride) {
+                const int64_t row = sg / a.segs;
+                const int64_t first = (sg - row * a.segs) * kCompressChunksPerSeg;
+                const int64_t n = min(static_cast<int64_t>(kCompressChunksPerSeg), a.row_chunks - first);
+                for (int h = 0; h * kHalfChunks < n; ++h, ++j) {
+                    const int st = j % kRingStages;
+                    if (!mbar_wait(&empty[st], ((j / kRingStages) & 1) ^ 1, wait_ns, abort_flag)) {
+                        *abort_flag = 1;
+                        flag_status(status, kDevTimeout);
+                        stop = true;
+                        break;
+                    }
+                    const int64_t c0 = first + h * kHalfChunks;
+                    const int64_t nh = min(static_cast<int64_t>(kHalfChunks), n - h * kHalfChunks);
+                    const uint32_t bytes = static_cast<uint32_t>(nh) * 16;
+                    uint8_t *dst = smem + st * 2 * kHalfBytes;
+                    mbar_arrive_expect_tx(&full[st], 2 * bytes);
+                    bulk_load(dst, a.wb + row * a.row_chunks + c0, bytes, &full[st]);
+                    bulk_load(dst + kHalfBytes, a.wf + row * a.row_chunks + c0, bytes, &full[st]);
+                    issued = j + 1;
+                }
+            }
+            if (*abort_flag) {
+                for (int q = (issued > kRingStages ? issued - kRingStages : 0); q < issued; ++q)
+                    mbar_wait(&full[q % kRingStages], (q / kRingStages) & 1, kDrainLimitNs, nullptr);
+            }
+        }
+        return;  // the producer takes no part in the consumers' barriers
+    }
+
+    int j = 0, seg_i = 0;
+    bool ok = true;
+    for (int64_t sg = first_seg; sg < n_segs_total && ok; sg += stride, ++seg_i) {
+        const int64_t row = sg / a.segs;
+        const int64_t first = (sg - row * a.segs) * kCompressChunksPerSeg;
+        const int64_t n = min(static_cast<int64_t>(kCompressChunksPerSeg), a.row_chunks - first);
+        uint8_t *bits = a.bits + row * a.row_chunks + first;
+        float cs[kCompressChunksPerThread];
 #pragma unroll
-        for (int w = 0; w < kCompressThreads / 32; ++w) s += warp_sum[w];
-        a.partials[seg_id] = s;
+        for (int u = 0; u < kCompressChunksPerThread; ++u) cs[u] = 0.0f;
+        for (int h = 0; h * kHalfChunks < n; ++h, ++j) {
+            const int st = j % kRingStages;
+            const bool got = mbar_wait(&full[st], (j / kRingStages) & 1, wait_ns, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    flag_status(status, kDevTimeout);
+                }
+                ok = false;
+                break;
+            }
+            const uint4 *sb = reinterpret_cast<const uint4 *>(smem + st * 2 * kHalfBytes);
+            const uint4 *sf = reinterpret_cast<const uint4 *>(smem + st * 2 * kHalfBytes + kHalfBytes);
+#pragma unroll
+            for (int uu = 0; uu < kCompressChunksPerThread / 2; ++uu) {
+                const int cl = uu * kCompressThreads + tid;        // chunk within this half
+                const int c = h * kHalfChunks + cl;                // chunk within the segment
+                if (c < n) {
+                    float sum;
+                    const uint32_t byte = chunk_signs(sb[cl], sf[cl], sum);
+                    bits[c] = static_cast<uint8_t>(byte);
+                    if (h == 0) cs[uu] = sum;
+                    else cs[uu + kCompressChunksPerThread / 2] = sum;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        // all consumer warps leave together on a timeout: the barrier below counts them all
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        const float t32 = ((cs[0] + cs[1]) + (cs[2] + cs[3])) + ((cs[4] + cs[5]) + (cs[6] + cs[7]));
+        double acc = static_cast<double>(t32);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        double *ws = warp_sum + (seg_i & 1) * 8;
+        if (lane == 0) ws[warp] = acc;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (!*abort_flag && tid == 0) {
+            double s = 0.0;
+#pragma unroll
+            for (int w = 0; w < kCompressThreads / 32; ++w) s += ws[w];
+            a.partials[sg] = s;
+        }
+        if (*abort_flag) break;
     }
 }
 
@@ -144,7 +234,6 @@ CompressGeom compress_geometry(int64_t n_out, int64_t n_in, int32_t alpha_mode) 
 
 cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out, int64_t n_in, int32_t alpha_mode,
                             uint8_t *bits, float *alpha, double *partials, const DevCtx &ctx, cudaStream_t stream) {
-    (void)ctx;
     const CompressGeom g = compress_geometry(n_out, n_in, alpha_mode);
     CompressArgs a;
     a.wb = static_cast<const uint4 *>(w_base);
@@ -153,10 +242,26 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
     a.partials = partials;
     a.row_chunks = g.row_chunks;
     a.segs = g.segs;
-    const int64_t blocks = g.rows * g.segs;
-    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    compress_pass1<<<static_cast<unsigned>(blocks), kCompressThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    const int64_t n_segs = g.rows * g.segs;
+    static bool attr_set[128] = {false};
+    if (ctx.device >= 0 && ctx.device < 128 && !attr_set[ctx.device]) {
+        cudaError_t e = cudaFuncSetAttribute(compress_pass1, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kPass1Smem));
+        if (e != cudaSuccess) return e;
+        attr_set[ctx.device] = true;
+    }
+    const int64_t grid = n_segs < 2 * ctx.num_sms ? n_segs : 2 * ctx.num_sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid > 0 ? grid : 1), 1, 1);
+    cfg.blockDim = dim3(kPass1Threads, 1, 1);
+    cfg.dynamicSmemBytes = kPass1Smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, compress_pass1, a, n_segs, ctx.status, ctx.wait_ns);
     if (e != cudaSuccess) return e;
     const double count = static_cast<double>(g.row_chunks) * 8.0;
     if (g.segs <= 32) {

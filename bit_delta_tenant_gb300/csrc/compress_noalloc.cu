@@ -65,15 +65,14 @@ BD_API int32_t bd_compress_noalloc(const void *w_base, const void *w_ft, int64_t
     const bd::CompressGeom g = bd::compress_geometry(n_out, n_in, alpha_mode);
     if (g.rows * g.segs > static_cast<int64_t>(BD_NOALLOC_MAX_PARTIALS)) return BD_ERR_WORKSPACE;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BD_ERR_CUDA;
     bd::DevCtx ctx;
-    double *partials = nullptr;
-    const int32_t rc = setup_device(dev, &partials, &ctx.num_sms);
+    int32_t rc = bd::make_dev_ctx(&ctx);  // status word and wait limit, as for bd_compress
     if (rc != BD_OK) return rc;
-    ctx.device = dev;
-    ctx.status = nullptr;  // compression has no bounded waits and no ids to check
-    ctx.wait_ns = 0;
+    if (ctx.device >= kMaxDevices) return BD_ERR_CUDA;
+    double *partials = nullptr;
+    int sms = 0;
+    rc = setup_device(ctx.device, &partials, &sms);
+    if (rc != BD_OK) return rc;
     // Every partial slot the kernels read is written earlier in the same call
     // (one slot per block of the first pass), so nothing needs clearing.
     const cudaError_t e = bd::launch_compress(w_base, w_ft, n_out, n_in, alpha_mode, bits_out, alpha_out, partials,

@@ -1,8 +1,8 @@
 // decode_tma.cu -- the HBM-streaming fused BitDelta linear for small token
 // counts, fed by TMA.  Same arithmetic as decode.cu (distributive form
 // y = x.W_base^T + alpha * (x.S^T) on mma.m16n8k16, signs built in registers),
-// but W_base and the packed bits arrive through a multi-stage ring of
-// shared-memory tiles filled by one producer warp with cp.async.bulk.tensor,
+// but W_base, the packed bits and the activations arrive through a multi-stage
+// ring of shared-memory tiles filled by one producer warp with cp.async.bulk.tensor,
 // so each SM keeps tens of KB of HBM reads in flight for a handful of
 // instructions, and two CTAs fit on an SM.
 //
@@ -13,8 +13,9 @@
 // listing).
 //
 // CTA: 8 consumer warps + 1 producer warp; 64 W rows; a stage is a 128-column
-// K step: two 64x64 bf16 W boxes (128-byte swizzle) and one 64x16-byte box of
-// packed bits.  Consumer warp w owns row group w%4 (16 rows, the M side of the
+// K step: two 64x64 bf16 W boxes (128-byte swizzle), one 64x16-byte box of
+// packed bits and two (8*NT tokens x 64 columns) activation boxes (128-byte
+// swizzle; rows beyond m arrive as zeros).  Consumer warp w owns row group w%4 (16 rows, the M side of the
 // MMA) and 64-column half w/4 of every stage.  Lane (g, t) reads 16-byte
 // chunks 2t and 2t+1 of rows g and g+8 -- with the swizzle the eight lanes of a
 // shared-memory phase hit eight different bank groups -- so its 16 columns are
@@ -41,31 +42,30 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 288
 constexpr int kRows = 64;                            // W rows per CTA
 constexpr int kStepK = 128;                          // K columns per stage
-constexpr int kStages = 4;
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;          // one 64-row x 64-column bf16 box
 constexpr uint32_t kBitsBytes = kRows * 16;          // 64 rows x 16 packed bytes (128 columns)
-constexpr uint32_t kStageBytes = 2 * kBoxBytes + kBitsBytes;
-constexpr int kMaxKs = 2048;                         // longest K slice staged per CTA
+
+// Per token-tile count NT (8 tokens each): ring depth, and the stage layout
+// [W box k0..63][W box k64..127][bits][x box k0..63][x box k64..127]; every box
+// starts on a 1024-byte boundary (the 128-byte swizzle pattern repeats there).
+template <int NT> struct Ring {
+    static constexpr int kStages = NT == 1 ? 5 : NT == 2 ? 4 : NT == 4 ? 7 : 6;
+    static constexpr uint32_t kXBox = 8 * NT * 128;  // MP tokens x 64 columns
+    static constexpr uint32_t kStageBytes = 2 * kBoxBytes + kBitsBytes + 2 * kXBox;
+    static constexpr uint32_t kRedBytes = 8 * NT * kRows * 4;
+    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + kRedBytes + 2 * kStages * 8 + 16;
+};
 
 struct TmaDecodeArgs {
-    const uint8_t *x;
     const float *alpha;
     uint16_t *y;
     int64_t m, n_out, n_in;
     int64_t ks;
     int32_t mode;
     int32_t cluster;
-    int32_t x_stride;
-    int32_t x_off;     // byte offset of the activation slice in shared memory
-    int32_t red_off;   // byte offset of the reduction buffers
     unsigned *status;
     uint64_t wait_ns;
 };
-
-__device__ __forceinline__ void pdl_trigger_and_wait() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -79,15 +79,17 @@ __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *stat
 template <int NT>
 __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
     decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
-                      const __grid_constant__ TmaDecodeArgs a) {
+                      const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ TmaDecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int MP = 8 * NT;
+    constexpr int kStages = Ring<NT>::kStages;
+    constexpr uint32_t kStageBytes = Ring<NT>::kStageBytes;
+    constexpr uint32_t kXBox = Ring<NT>::kXBox;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    float *red = reinterpret_cast<float *>(smem + kStages * kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes + Ring<NT>::kRedBytes);
     uint64_t *empty = full + kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
-    uint8_t *xs = smem + a.x_off;
-    float *red = reinterpret_cast<float *>(smem + a.red_off);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
         if (lane == 0) {
             tma_prefetch_desc(&tm_w);
             tma_prefetch_desc(&tm_b);
+            tma_prefetch_desc(&tm_x);
             int issued = 0;
             for (int i = 0; i < n_steps; ++i) {
                 const int s = i % kStages;
@@ -140,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
                 tma_load_2d(st, &tm_w, &full[s], kc, row0);
                 tma_load_2d(st + kBoxBytes, &tm_w, &full[s], kc + 64, row0);
                 tma_load_2d(st + 2 * kBoxBytes, &tm_b, &full[s], kc / 8, row0);
+                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes, &tm_x, &full[s], kc, 0);
+                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes + kXBox, &tm_x, &full[s], kc + 64, 0);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -148,18 +153,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
             }
         }
     } else {
-        // ---- consumers: stage x[:, k_lo : k_lo + ks] (zero beyond m and n_in) ----
-        const int vec_per_row = static_cast<int>(a.ks / 8);
-        for (int i = threadIdx.x; i < MP * vec_per_row; i += kConsumerWarps * 32) {
-            const int r = i / vec_per_row;
-            const int c = i - r * vec_per_row;
-            const int64_t k = k_lo + static_cast<int64_t>(c) * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < a.m && k < k_hi) v = ldg_keep(a.x + (static_cast<int64_t>(r) * a.n_in + k) * 2);
-            *reinterpret_cast<uint4 *>(xs + r * a.x_stride + c * 16) = v;
-        }
-        consumer_sync();
-
+        // ---- consumers ----
+        // Token rows of the x boxes use the same swizzle term as W rows: (8*tt + g) & 7 == r0 & 7 == g.
         const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ (r0 & 7)) << 4);
         const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ (r0 & 7)) << 4);  // rows r0, r0+8 share r&7
         for (int i = 0; i < n_steps; ++i) {
@@ -189,11 +184,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
                                     sign_pair_bf16<2>(bb1), sign_pair_bf16<3>(bb1)};
             const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
             const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
-            const uint8_t *xrow = xs + (i * kStepK + kh * 64 + 16 * t) * 2 + g * a.x_stride;
+            const uint8_t *xrow = st + 2 * kBoxBytes + kBitsBytes + kh * kXBox + g * 128;
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt) {
-                const uint4 p0 = lds128(xrow + 8 * tt * a.x_stride);
-                const uint4 p1 = lds128(xrow + 8 * tt * a.x_stride + 16);
+                const uint4 p0 = lds128(xrow + tt * 1024 + sw0);
+                const uint4 p1 = lds128(xrow + tt * 1024 + sw1);
                 const uint32_t xv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -220,9 +215,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
             part[tt][2] = accb[tt][2] + al1 * accs[tt][2];
             part[tt][3] = accb[tt][3] + al1 * accs[tt][3];
         }
-        // red[token][row] may reuse the activation slice: wait until every consumer is past it.
-        // The upper half writes, the lower half adds its own and keeps the sum.
-        consumer_sync();
+        // red[token][row]: the upper half writes, the lower half adds its own and keeps the sum.
         if (kh == 1) {
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt) {
@@ -265,9 +258,8 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
 }
 
 struct TmaPlan {
-    int nt, cluster, x_stride;
+    int nt, cluster;
     int64_t ks, row_blocks;
-    size_t x_off, red_off, smem;
 };
 
 int env_int(const char *name, int dflt) {
@@ -280,54 +272,39 @@ int env_int(const char *name, int dflt) {
 bool make_tma_plan(int64_t m, int64_t n_out, int64_t n_in, int num_sms, TmaPlan &p) {
     if (m < 1 || m > kDecodeMaxM) return false;
     p.nt = m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8;
-    const int mp = 8 * p.nt;
     p.row_blocks = (n_out + kRows - 1) / kRows;
-    const int slots = (p.nt <= 2 ? 2 : 1) * num_sms;
-    int c = static_cast<int>((2 * static_cast<int64_t>(slots) + p.row_blocks - 1) / p.row_blocks);
+    // Split K over a cluster only when the 64-row blocks alone leave SMs idle:
+    // each split adds a reduction, an activation re-read and cluster placement
+    // constraints.  Measured on GB300: one split when row blocks >= SMs; about
+    // 1.5 CTAs per SM otherwise (4096 rows -> 4 splits).
+    int c = 1;
+    if (p.row_blocks < num_sms)
+        c = static_cast<int>((3 * static_cast<int64_t>(num_sms) / 2 + p.row_blocks - 1) / p.row_blocks);
     c = env_int("BD_DECODE_CLUSTER", c);
     if (c < 1) c = 1;
     if (c > 8) c = 8;
-    // Shared memory: the ring, the activation slice, the reduction buffer (which
-    // reuses the slice when that is large enough).  Prefer a K split that keeps
-    // two CTAs per SM for the small token tiles; otherwise any that fits.
-    const size_t ring = static_cast<size_t>(kStages) * kStageBytes + 2 * kStages * sizeof(uint64_t) + 16;
-    const size_t x_off = (ring + 127) & ~size_t(127);
-    const size_t rbytes = static_cast<size_t>(mp) * kRows * sizeof(float);
-    for (size_t limit : {p.nt <= 2 ? size_t(112 * 1024) : size_t(227 * 1024), size_t(227 * 1024)}) {
-        for (int cc = c; cc <= 8; ++cc) {
-            int64_t ks = (n_in + cc - 1) / cc;
-            ks = (ks + kStepK - 1) / kStepK * kStepK;
-            if (ks > kMaxKs) continue;
-            const int x_stride = static_cast<int>(ks * 2 + 16);
-            const size_t xbytes = static_cast<size_t>(mp) * x_stride;
-            const size_t end = xbytes >= rbytes ? x_off + xbytes : x_off + xbytes + rbytes;
-            if (1024 + end > limit) continue;
-            p.cluster = static_cast<int>((n_in + ks - 1) / ks);  // no empty ranks
-            p.ks = ks;
-            p.x_stride = x_stride;
-            p.x_off = x_off;
-            p.red_off = xbytes >= rbytes ? x_off : x_off + xbytes;
-            p.smem = 1024 + end;
-            return true;
-        }
-    }
-    return false;
+    const int64_t steps = (n_in + kStepK - 1) / kStepK;
+    if (c > steps) c = static_cast<int>(steps);
+    const int64_t per = (steps + c - 1) / c;
+    p.ks = per * kStepK;
+    p.cluster = static_cast<int>((steps + per - 1) / per);  // no empty ranks
+    return true;
 }
 
 template <int NT>
-cudaError_t launch_nt(const CUtensorMap &tw, const CUtensorMap &tb, const TmaDecodeArgs &a, const TmaPlan &p,
-                      const DevCtx &ctx, cudaStream_t stream) {
+cudaError_t launch_nt(const CUtensorMap &tw, const CUtensorMap &tb, const CUtensorMap &tx, const TmaDecodeArgs &a,
+                      const TmaPlan &p, const DevCtx &ctx, cudaStream_t stream) {
     static bool attr_set[128] = {false};
     if (ctx.device < 128 && !attr_set[ctx.device]) {
         cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             227 * 1024);
+                                             static_cast<int>(Ring<NT>::kSmem));
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.row_blocks * p.cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = p.smem;
+    cfg.dynamicSmemBytes = Ring<NT>::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -338,7 +315,7 @@ cudaError_t launch_nt(const CUtensorMap &tw, const CUtensorMap &tb, const TmaDec
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_tma_kernel<NT>, tw, tb, a);
+    return cudaLaunchKernelEx(&cfg, decode_tma_kernel<NT>, tw, tb, tx, a);
 }
 
 }  // namespace
@@ -347,6 +324,7 @@ bool decode_tma_supported(int64_t m, int64_t n_out, int64_t n_in, const void *w_
                           int num_sms) {
     if (n_in % kStepK != 0) return false;  // packed-bit rows must be 16-byte multiples for TMA
     if ((reinterpret_cast<uintptr_t>(w_base) & 15) || (reinterpret_cast<uintptr_t>(bits) & 15)) return false;
+    if (n_in >= (int64_t(1) << 31) - kStepK) return false;
     TmaPlan p;
     return make_tma_plan(m, n_out, n_in, num_sms, p);
 }
@@ -364,8 +342,12 @@ cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, cons
     if (!encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bits, n_in / 8, n_out, n_in / 8, 16, kRows,
                               CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
+    const int mp = 8 * p.nt;
+    CUtensorMap tx;
+    if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, m, n_in * 2, 64,
+                              static_cast<uint32_t>(mp), CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     TmaDecodeArgs a;
-    a.x = static_cast<const uint8_t *>(x);
     a.alpha = alpha;
     a.y = static_cast<uint16_t *>(y);
     a.m = m;
@@ -374,16 +356,13 @@ cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, cons
     a.ks = p.ks;
     a.mode = alpha_mode;
     a.cluster = p.cluster;
-    a.x_stride = p.x_stride;
-    a.x_off = static_cast<int32_t>(p.x_off);
-    a.red_off = static_cast<int32_t>(p.red_off);
     a.status = ctx.status;
     a.wait_ns = ctx.wait_ns;
     switch (p.nt) {
-        case 1: return launch_nt<1>(tw, tb, a, p, ctx, stream);
-        case 2: return launch_nt<2>(tw, tb, a, p, ctx, stream);
-        case 4: return launch_nt<4>(tw, tb, a, p, ctx, stream);
-        default: return launch_nt<8>(tw, tb, a, p, ctx, stream);
+        case 1: return launch_nt<1>(tw, tb, tx, a, p, ctx, stream);
+        case 2: return launch_nt<2>(tw, tb, tx, a, p, ctx, stream);
+        case 4: return launch_nt<4>(tw, tb, tx, a, p, ctx, stream);
+        default: return launch_nt<8>(tw, tb, tx, a, p, ctx, stream);
     }
 }
 

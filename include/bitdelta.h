@@ -78,9 +78,9 @@ typedef enum bd_alpha_mode {
  * fp32 from the bf16 inputs).  Writes the packed sign bits and alpha:
  *   scalar:  alpha[0] = sum_{j,k} |Delta_jk| / (n_out * n_in)
  *   per-row: alpha[j] = sum_k |Delta_jk| / n_in
- * The sums use fp32 partials over 8 elements, widened to fp64 and reduced
- * in a fixed order, so alpha is bitwise reproducible for a given
- * shape, and is rounded once to fp32 at the end.
+ * The sums use pairwise fp32 partials over at most 64 elements, widened to
+ * fp64 and reduced in a fixed order (relative error below 5e-7), so alpha is
+ * bitwise reproducible for a given shape, and is rounded once to fp32.
  *
  *   w_base, w_ft  bf16 [n_out, n_in]   (read)
  *   bits_out      uint8 [n_out, n_in/8] (written)
