@@ -13,19 +13,26 @@
 //   warp 0      TMA producer: per 64-wide K block, the W_base tile
 //               [128 x 64] and the x tile [256 x 64], both K-major with the
 //               128-byte swizzle, into a 4-stage ring.
-//   warps 2..5  reconstruction: thread r owns tile row r; it reads the row's
-//               8 packed bytes for the K block (prefetched two blocks ahead),
-//               and rewrites each 16-byte chunk of the swizzled W tile in
-//               place as bf16(fp32(W_base) + alpha_r * s) -- one chunk is
-//               exactly one packed byte.  After the K loop the same warps are
-//               the epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
-//   warp 1      allocates 256 TMEM columns; lane 0 issues
-//               tcgen05.mma kind::f16 (M=128, N=256, K=16, bf16 in, fp32
-//               accumulate in TMEM) on the reconstructed tile and commits
-//               each stage back to the producer.
+//   warps 2..9  reconstruction: two threads per tile row, each with half of
+//               the row's 8 packed bytes for the K block (prefetched two
+//               blocks ahead); each rebuilds its four 16-byte chunks of the
+//               swizzled W tile as bf16(fp32(W_base) + alpha_r * s) -- one
+//               chunk is exactly one packed byte.  After the K loop the same
+//               warps are the epilogue (warp w reads TMEM lanes 32*(w%4)..+31,
+//               two warps per lane quarter splitting the token columns).
+//   warp 1      allocates TMEM (256 accumulator columns, plus 32 columns per
+//               stage for the rebuilt A tile); lane 0 issues tcgen05.mma
+//               kind::f16 (M=128, N=tokens<=256, K=16, bf16 in, fp32
+//               accumulate in TMEM) and commits each stage back to the producer.
+// The rebuilt tile goes from registers to tensor memory (tcgen05.st) and the
+// MMA takes A from there, so shared memory carries only the TMA fills, the
+// rebuild reads and the activation (B) operand; with BD_PREFILL_TMEM_A=0 the
+// tile is instead written back in place and read by the MMA from shared memory.
 // Every wait is bounded; a role that gives up records a timeout in the status
 // word, tells the other roles through a shared flag, drains its own copies
 // and MMAs in flight, and the CTA frees its TMEM and returns.
+#include <cstdlib>
+
 #include "bd_device.cuh"
 #include "bd_internal.h"
 
@@ -39,8 +46,9 @@ constexpr int kStages = 4;
 constexpr uint32_t kWBytes = kBM * kBK * 2;
 constexpr uint32_t kXBytes = kBN * kBK * 2;
 constexpr uint32_t kStageTx = kWBytes + kXBytes;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kRebuildWarps = 8;
+constexpr int kThreads = (2 + kRebuildWarps) * 32;  // producer, MMA issuer, rebuild/epilogue
+constexpr uint32_t kAccCols = 256;  // fp32 accumulator columns (one per token)
 constexpr size_t kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 256;
 constexpr int kMaxVariants = 64;
 
@@ -67,9 +75,14 @@ struct PrefillArgs {
     int32_t vmode[kMaxVariants];
 };
 
-__device__ __forceinline__ uint32_t rebuild_pair(uint32_t w, uint32_t byte, int i, float al) {
-    const float lo = bf16lo_to_f32(w) + (((byte >> (2 * i)) & 1u) ? al : -al);
-    const float hi = bf16hi_to_f32(w) + (((byte >> (2 * i + 1)) & 1u) ? al : -al);
+// One bf16 pair of W_eff = bf16(fp32(W_base) + alpha * s): the sign bit of
+// -alpha is cleared where the packed bit is 1 (+alpha) and kept where it is 0.
+template <int I>
+__device__ __forceinline__ uint32_t rebuild_pair(uint32_t w, uint32_t byte, uint32_t neg_alpha_bits) {
+    const uint32_t s_lo = ((byte << (31 - 2 * I)) & 0x80000000u) ^ neg_alpha_bits;
+    const uint32_t s_hi = ((byte << (30 - 2 * I)) & 0x80000000u) ^ neg_alpha_bits;
+    const float lo = bf16lo_to_f32(w) + __uint_as_float(s_lo);
+    const float hi = bf16hi_to_f32(w) + __uint_as_float(s_hi);
     return pack_bf16x2(lo, hi);
 }
 
@@ -78,11 +91,14 @@ __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *stat
     flag_status(status, kDevTimeout);
 }
 
-template <bool kGrouped>
+template <bool kGrouped, bool kTmemA>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
+    // With kTmemA the rebuilt W tile goes to tensor memory (columns 256 + 32*stage)
+    // and the MMA reads A from there; otherwise it is written back in place.
+    constexpr uint32_t kTmemCols = kTmemA ? 512 : 256;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;
     uint8_t *sX = smem + kStages * kWBytes;
@@ -138,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&rebuilt[s], 4);
+            mbar_init(&rebuilt[s], kRebuildWarps);
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
@@ -194,8 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t b_addr = smem_u32(sX + s * kXBytes);
 #pragma unroll
                 for (int kk = 0; kk < kBK / 16; ++kk) {
-                    tc_mma_f16_ss(tmem, sw128_kmajor_desc(a_addr + kk * 32), sw128_kmajor_desc(b_addr + kk * 32),
-                                  idesc, (kb | kk) != 0 ? 1u : 0u);
+                    if constexpr (kTmemA)
+                        tc_mma_f16_ts(tmem, tmem + kAccCols + s * (kBK / 2) + kk * 8,
+                                      sw128_kmajor_desc(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+                    else
+                        tc_mma_f16_ss(tmem, sw128_kmajor_desc(a_addr + kk * 32),
+                                      sw128_kmajor_desc(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
                 }
                 tc_commit(&empty[s]);
             }
@@ -206,43 +226,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(acc_full, 0, kDrainLimitNs, nullptr);
         }
     } else {
-        // ---- reconstruction (then epilogue) warps --------------------------------------
-        const int sub = warp & 3;  // TMEM lane quarter this warp may access
+        // ---- rebuild (then epilogue) warps ------------------------------------------
+        // Thread q owns tile row r = 32*(warp%4) + lane and chunk pair h (0..3):
+        // the 16-byte chunks 2h, 2h+1 of the row in every K block (two packed
+        // bytes).  Warp w may read TMEM lanes 32*(w%4)..+31 only, so the same
+        // row mapping serves the epilogue, where h picks a quarter of the tokens.
+        constexpr int kParts = kRebuildWarps / 4;        // threads per row
+        constexpr int kChunks = 8 / kParts;              // chunks per thread per K block
+        const int sub = warp & 3;
+        const int h = (warp - 2) >> 2;
         const int r = sub * 32 + lane;
         const int64_t row = static_cast<int64_t>(m0) + r;
         const bool row_ok = row < a.n_out;
         const float al = row_ok ? (mode ? alpha[row] : alpha[0]) : 0.0f;
+        const uint32_t neg_al = __float_as_uint(-al);
         const int64_t bpr = a.n_in / 8;
-        const uint8_t *brow = bits + (row_ok ? row : 0) * bpr;
+        const uint8_t *brow = bits + (row_ok ? row : 0) * bpr + kChunks * h;
 
-        auto load_bits = [&](int kb) -> uint2 {
-            uint2 v = make_uint2(0u, 0u);
+        auto load_bits = [&](int kb) -> uint32_t {
+            uint32_t v = 0;
             if (row_ok && kb < nkb) {
-                const int64_t c0 = static_cast<int64_t>(kb) * 8;
-                if (a.bits_vec8 && c0 + 8 <= bpr) {
-                    v = __ldg(reinterpret_cast<const uint2 *>(brow + c0));
+                const int64_t c0 = static_cast<int64_t>(kb) * 8 + kChunks * h;  // first packed byte
+                if (a.bits_vec8 && c0 + kChunks <= bpr) {
+                    const uint8_t *q = brow + static_cast<int64_t>(kb) * 8;
+                    if constexpr (kChunks == 4) v = __ldg(reinterpret_cast<const uint32_t *>(q));
+                    else if constexpr (kChunks == 2) v = __ldg(reinterpret_cast<const uint16_t *>(q));
+                    else v = __ldg(q);
                 } else {
-                    uint32_t lo = 0, hi = 0;
-                    for (int c = 0; c < 8; ++c) {
-                        if (c0 + c < bpr) {
-                            const uint32_t b = __ldg(brow + c0 + c);
-                            if (c < 4) lo |= b << (8 * c);
-                            else hi |= b << (8 * (c - 4));
-                        }
-                    }
-                    v = make_uint2(lo, hi);
+                    for (int c = 0; c < kChunks; ++c)
+                        if (c0 + c < bpr)
+                            v |= static_cast<uint32_t>(__ldg(brow + static_cast<int64_t>(kb) * 8 + c)) << (8 * c);
                 }
             }
             return v;
         };
 
-        uint2 b_cur = load_bits(0);
-        uint2 b_nxt = load_bits(1);
+        uint32_t b_cur = load_bits(0);
+        uint32_t b_nxt = load_bits(1);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
             const int s = kb % kStages;
             const uint32_t ph = (kb / kStages) & 1;
-            const uint2 b_nn = load_bits(kb + 2);
+            const uint32_t b_nn = load_bits(kb + 2);
             const bool got = mbar_wait(&full[s], ph, a.wait_ns, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 if (lane == 0) give_up(abort_flag, a.status);
@@ -250,18 +275,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             uint8_t *rowp = sW + s * kWBytes + r * 128;
+            uint4 *p[kChunks];
+            uint4 w[kChunks];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t byte = ((c < 4 ? b_cur.x : b_cur.y) >> (8 * (c & 3))) & 0xFFu;
-                uint4 *p = reinterpret_cast<uint4 *>(rowp + ((c ^ (r & 7)) << 4));
-                uint4 w = *p;
-                w.x = rebuild_pair(w.x, byte, 0, al);
-                w.y = rebuild_pair(w.y, byte, 1, al);
-                w.z = rebuild_pair(w.z, byte, 2, al);
-                w.w = rebuild_pair(w.w, byte, 3, al);
-                *p = w;
+            for (int cc = 0; cc < kChunks; ++cc) {
+                p[cc] = reinterpret_cast<uint4 *>(rowp + (((kChunks * h + cc) ^ (r & 7)) << 4));
+                w[cc] = *p[cc];
             }
-            fence_proxy_async_smem();
+#pragma unroll
+            for (int cc = 0; cc < kChunks; ++cc) {
+                const uint32_t byte = (b_cur >> (8 * cc)) & 0xFFu;
+                w[cc].x = rebuild_pair<0>(w[cc].x, byte, neg_al);
+                w[cc].y = rebuild_pair<1>(w[cc].y, byte, neg_al);
+                w[cc].z = rebuild_pair<2>(w[cc].z, byte, neg_al);
+                w[cc].w = rebuild_pair<3>(w[cc].w, byte, neg_al);
+                if constexpr (!kTmemA) *p[cc] = w[cc];
+            }
+            if constexpr (kTmemA) {
+                static_assert(kChunks == 4, "one 16-column TMEM store per thread and K block");
+                const uint32_t v[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
+                                        w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
+                tmem_st_32x32b_x16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + kAccCols + s * (kBK / 2) +
+                                       16 * h,
+                                   v);
+                tmem_st_wait();
+                tc_fence_before();
+            } else {
+                fence_proxy_async_smem();
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&rebuilt[s]);
             b_cur = b_nxt;
@@ -275,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sub * 32) << 16);
                 uint16_t *ycol = a.y + row;
 #pragma unroll 1
-                for (int c0 = 0; c0 < kBN; c0 += 32) {
+                for (int c0 = h * (kBN / kParts); c0 < (h + 1) * (kBN / kParts); c0 += 32) {
                     if (c0 >= count) break;  // warp-uniform
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(lane_addr + c0, v);
@@ -286,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c0 + i < count) {
                                 const int64_t t = kGrouped ? static_cast<int64_t>(a.perm[n0 + c0 + i])
                                                            : static_cast<int64_t>(n0) + c0 + i;
-                                __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[i]));
-                                ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&h);
+                                __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[i]));
+                                ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&hv);
                             }
                         }
                     }
@@ -308,16 +349,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <bool kGrouped>
+template <bool kGrouped, bool kTmemA>
 cudaError_t set_smem_attr(const DevCtx &ctx) {
     static bool attr_set[128] = {false};
     if (ctx.device < 128 && !attr_set[ctx.device]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kGrouped>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kGrouped, kTmemA>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
     return cudaSuccess;
+}
+
+// The rebuilt W tile feeds the MMA from tensor memory by default (measured
+// ~19% faster on GB300 than writing it back to shared memory, which then
+// carries only the TMA fills, the rebuild reads and the activation operand);
+// BD_PREFILL_TMEM_A=0 selects the shared-memory form.
+bool use_tmem_a() {
+    static const bool v = [] {
+        const char *e = std::getenv("BD_PREFILL_TMEM_A");
+        return !(e != nullptr && e[0] == '0');
+    }();
+    return v;
 }
 
 void fill_common(PrefillArgs &a, int64_t m, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx) {
@@ -344,7 +397,8 @@ bool make_maps(CUtensorMap &tm_w, CUtensorMap &tm_x, const void *w_base, const v
 cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                            int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                            cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<false>(ctx);
+    const bool tmem_a = use_tmem_a();
+    cudaError_t e = tmem_a ? set_smem_attr<false, true>(ctx) : set_smem_attr<false, false>(ctx);
     if (e != cudaSuccess) return e;
     CUtensorMap tm_w, tm_x;
     if (!make_maps(tm_w, tm_x, w_base, x, m, n_out, n_in)) return cudaErrorInvalidValue;
@@ -358,14 +412,18 @@ cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const u
     a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
     const int64_t tiles = static_cast<int64_t>(a.row_tiles) * a.tok_tiles;
     if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    prefill_kernel<false><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+    if (tmem_a)
+        prefill_kernel<false, true><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+    else
+        prefill_kernel<false, false><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
                                    int64_t n_out, int64_t n_in, void *y, const GroupTable &tab, const DevCtx &ctx,
                                    cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<true>(ctx);
+    const bool tmem_a = use_tmem_a();
+    cudaError_t e = tmem_a ? set_smem_attr<true, true>(ctx) : set_smem_attr<true, false>(ctx);
     if (e != cudaSuccess) return e;
     CUtensorMap tm_w, tm_x;
     if (!make_maps(tm_w, tm_x, w_base, x_sorted, m, n_out, n_in)) return cudaErrorInvalidValue;
@@ -385,7 +443,10 @@ cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *
     a.max_slots = tab.max_slots;
     const int64_t grid = static_cast<int64_t>(a.row_tiles) * tab.max_slots;
     if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    prefill_kernel<true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+    if (tmem_a)
+        prefill_kernel<true, true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+    else
+        prefill_kernel<true, false><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
     return cudaGetLastError();
 }
 
