@@ -182,75 +182,189 @@ def decode_bytes(m, n_out, n_in, mode):
     return 2.0 * n_out * n_in + n_out * n_in / 8 + 4.0 * (n_out if mode == 1 else 1) + 2.0 * m * n_in + 2.0 * m * n_out
 
 
-class LayerDecode:
-    """Llama-7B-style layer linears at decode sizes (the default workload)."""
-    cfg = workloads.LLAMA7B_LAYER
+class Workload:
+    """Matrices, phases (each a list of C-ABI calls), e2e buffers and an oracle sample.
+
+    `value` of the JSON line = the step's work in `metric_unit` (algorithmic bytes
+    for GB/s, 2*m*N*K flops for TFLOP/s) / step time; phases measured in the
+    other unit still count in the time.
+    """
     metric_unit = "GB/s"
 
-    def __init__(self, bd, dev):
-        c = self.cfg
-        self.mats = [synth.matrix_pair(n_out, n_in, c["sigma"], c["b"], workloads.matrix_seed(c["seed"], i), dev)
-                     for i, (_, n_out, n_in) in enumerate(c["matrices"])]
-        self.comp, self.packed = compress_phase(bd, self.mats, c["mode"], dev)
-        self.xs, self.ys, calls, nbytes = {}, {}, [], 0.0
-        for m in c["ms"]:
-            for i, (name, n_out, n_in) in enumerate(c["matrices"]):
-                x = synth.activations(m, n_in, 10_000 + 97 * i + m, dev)
-                y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
-                self.xs[(m, i)], self.ys[(m, i)] = x, y
-                wb = self.mats[i][0]
-                bits, alpha = self.packed[i]
-                calls.append(lambda x=x, wb=wb, bits=bits, alpha=alpha, y=y:
-                             bd.bd_linear(x, wb, bits, alpha, c["mode"], y))
-                nbytes += decode_bytes(m, n_out, n_in, c["mode"])
-        self.dec = Phase("decode", calls, bytes_=nbytes, launches=len(calls))
-        self.phases = [self.comp, self.dec]
-        self.dominant = self.dec
-        self.config = {"workload": c["name"], "matrices": [f"{n}:{a}x{b}" for n, a, b in c["matrices"]],
-                       "tokens": list(c["ms"]), "alpha": "scalar", "dtype_in": "bf16 weights/activations",
-                       "l2": "inputs larger than L2 (~1.2 GB touched per step; two uses of a matrix are "
-                             "separated by >250 MB of other traffic)"}
-
-    def step_bytes(self):
-        return sum(p.bytes for p in self.phases)
+    def step_work(self):
+        if self.metric_unit == "GB/s":
+            return sum(p.bytes for p in self.phases if p.bound == "hbm")
+        return sum(p.flops for p in self.phases if p.bound == "tensor") / 1e3  # TFLOP/s with the GB/s scaling
 
     def e2e_buffers(self):
-        """Per-step host->device inputs (activations, fine-tuned weights) and device->host results."""
-        h2d = [(torch.empty_like(wf, device="cpu").pin_memory(), wf) for (_, wf) in self.mats]
-        h2d += [(torch.empty_like(x, device="cpu").pin_memory(), x) for x in self.xs.values()]
+        """Per-step host->device inputs (fine-tuned weights, activations) and device->host results."""
+        h2d = [(torch.empty_like(t, device="cpu").pin_memory(), t) for t in self.h2d_tensors]
         for host, devt in h2d:
             host.copy_(devt)
-        d2h = [(torch.empty_like(y, device="cpu").pin_memory(), y) for y in self.ys.values()]
-        d2h += [(torch.empty_like(a, device="cpu").pin_memory(), a) for (_, a) in self.packed]
+        d2h = [(torch.empty_like(t, device="cpu").pin_memory(), t) for t in self.d2h_tensors]
         return h2d, d2h
 
+
+class LayerWorkload(Workload):
+    """Every matrix of `cfg` compressed, then its fused linear at every m of `ms`.
+
+    Used for the Llama-7B layer at decode sizes (the default), the 70B-shape
+    prefill linears and the Llama-3-8B-shape stack (decode or prefill)."""
+
+    def __init__(self, bd, dev, cfg, ms, unit, name, layers=1, private_io=True):
+        self.cfg, self.metric_unit = cfg, unit
+        mode = cfg["mode"]
+        shapes = [(f"L{l}.{n}", a, b) for l in range(layers) for (n, a, b) in cfg["matrices"]]
+        self.shapes = shapes
+        self.mats = [synth.matrix_pair(n_out, n_in, cfg["sigma"], cfg["b"], workloads.matrix_seed(cfg["seed"], i), dev)
+                     for i, (_, n_out, n_in) in enumerate(shapes)]
+        self.comp, self.packed = compress_phase(bd, self.mats, mode, dev)
+        self.xs, self.ys = {}, {}
+        calls, nbytes, flops = [], 0.0, 0.0
+        for m in ms:
+            for i, (_, n_out, n_in) in enumerate(shapes):
+                xk = (m, i) if private_io else (m, n_in)
+                yk = (m, i) if private_io else (m, n_out)
+                if xk not in self.xs:
+                    self.xs[xk] = synth.activations(m, n_in, 10_000 + 97 * len(self.xs) + m, dev)
+                if yk not in self.ys:
+                    self.ys[yk] = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+                x, y = self.xs[xk], self.ys[yk]
+                wb = self.mats[i][0]
+                bits, alpha = self.packed[i]
+                calls.append(lambda x=x, wb=wb, bits=bits, alpha=alpha, y=y: bd.bd_linear(x, wb, bits, alpha, mode, y))
+                nbytes += decode_bytes(m, n_out, n_in, mode)
+                flops += 2.0 * m * n_out * n_in
+        bound = "hbm" if unit == "GB/s" else "tensor"
+        self.lin = Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=len(calls), bound=bound)
+        self.phases = [self.comp, self.lin]
+        self.dominant = self.lin
+        self.h2d_tensors = [wf for (_, wf) in self.mats] + list(self.xs.values())
+        self.d2h_tensors = list(self.ys.values()) + [a for (_, a) in self.packed]
+        self.config = {"workload": name, "matrices": sorted({f"{a}x{b}" for _, a, b in shapes}),
+                       "matrix_count": len(shapes), "tokens": list(ms),
+                       "alpha": "per-row" if mode == 1 else "scalar", "dtype_in": "bf16 weights/activations",
+                       "l2": "inputs larger than L2 (consecutive uses of a matrix separated by >250 MB of traffic)"}
+
     def oracle_sample(self, oracle, frac_rows: float):
-        """Bounded CPU sample of one step: the first `frac_rows` of every matrix's rows."""
-        c = self.cfg
+        """Bounded CPU sample of one step: the first `frac_rows` of the first layer's rows."""
+        cfg = self.cfg
+        mode = cfg["mode"]
+        first_layer = len(cfg["matrices"])
         host = []
-        for i, (wb, wf) in enumerate(self.mats):
+        for i, (wb, wf) in enumerate(self.mats[:first_layer]):
             n = max(8, int(wb.shape[0] * frac_rows))
             host.append((synth.as_u16(wb[:n]), synth.as_u16(wf[:n])))
-        xs = {k: synth.as_u16(v) for k, v in self.xs.items()}
+        ms = sorted({k[0] for k in self.xs})
+        tok_cap = 64  # at most the first 64 tokens of each batch (prefill batches are thousands)
+        xs = {}
+        for m in ms:
+            for i, (_, _, n_in) in enumerate(self.shapes[:first_layer]):
+                key = (m, i) if (m, i) in self.xs else (m, n_in)
+                xs[(m, i)] = synth.as_u16(self.xs[key][:tok_cap])
 
         def run():
-            nbytes = 0.0
+            nbytes, flops = 0.0, 0.0
             packed = []
             for (wb, wf) in host:
-                bits, a32, _ = oracle.compress(wb, wf, c["mode"])
+                bits, a32, _ = oracle.compress(wb, wf, mode)
                 packed.append((bits, a32))
                 nbytes += 4.0 * wb.size + wb.size / 8 + 4.0
             for (m, i), x in xs.items():
                 wb = host[i][0]
                 bits, a32 = packed[i]
-                oracle.linear(x, wb, bits, a32, c["mode"])
-                nbytes += decode_bytes(m, wb.shape[0], wb.shape[1], c["mode"])
-            return nbytes
-        desc = f"every matrix's first {frac_rows:.4g} of rows: compress + fused linear at m=1,4,16"
+                oracle.linear(x, wb, bits, a32, mode)
+                nbytes += decode_bytes(x.shape[0], wb.shape[0], wb.shape[1], mode)
+                flops += 2.0 * x.shape[0] * wb.shape[0] * wb.shape[1]
+            return nbytes if self.metric_unit == "GB/s" else flops / 1e3
+        desc = (f"first layer, each matrix's first {frac_rows:.4g} of rows: compression + fused linear "
+                f"at m={','.join(str(min(m, tok_cap)) for m in ms)} (first tokens of each batch)")
         return run, desc
 
 
-WORKLOADS = {"llama7b_layer_decode": LayerDecode}
+class GroupedWorkload(Workload):
+    """14 variants over one 8192x8192 base: compress every variant, then one
+    multi-tenant linear (64 decode tokens with uniform ids, or 2048 prefill
+    tokens in Zipf(1.1) segments)."""
+
+    def __init__(self, bd, dev, kind):
+        c = workloads.GROUPED_14
+        self.cfg, self.kind = c, kind
+        self.metric_unit = "GB/s" if kind == "decode" else "TFLOP/s"
+        n_out, n_in, nv = c["n_out"], c["n_in"], c["n_variants"]
+        g = synth.generator(c["seed"], dev)
+        self.w_base = synth.bf16_normal((n_out, n_in), c["sigma"], g, dev)
+        self.fts = []
+        for v, b in enumerate(workloads.variant_scales(c)):
+            d = synth.laplace_f32((n_out, n_in), b, g, dev)
+            self.fts.append((self.w_base.float() + d).to(torch.bfloat16))
+            del d
+        self.mats = [(self.w_base, wf) for wf in self.fts]
+        self.comp, self.packed = compress_phase(bd, self.mats, c["mode"], dev)
+        m = c["decode_m"] if kind == "decode" else c["prefill_m"]
+        ids = synth.uniform_ids(m, nv, c["seed"]) if kind == "decode" else synth.zipf_ids(m, nv, c["zipf_s"], c["seed"])
+        self.ids_h = ids
+        self.ids = torch.from_numpy(ids).to(dev)
+        self.x = synth.activations(m, n_in, c["seed"] + 1, dev)
+        self.y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty((bd.bd_linear_grouped_workspace_size(m, nv, n_out, n_in),), dtype=torch.uint8, device=dev)
+        bits_v = [b for b, _ in self.packed]
+        alpha_v = [a for _, a in self.packed]
+        modes = [c["mode"]] * nv
+        call = lambda: bd.bd_linear_grouped(self.x, self.ids, self.w_base, bits_v, alpha_v, modes, self.y, self.ws)
+        active = len(set(ids.tolist()))
+        nbytes = 2.0 * n_out * n_in + active * n_out * n_in / 8 + 4.0 * nv + 2.0 * m * n_in + 2.0 * m * n_out
+        flops = 2.0 * m * n_out * n_in
+        bound = "hbm" if kind == "decode" else "tensor"
+        # the sort and gather kernels are tiny; the launch count is the library's whole call
+        self.lin = Phase("grouped_linear", [call], bytes_=nbytes, flops=flops, launches=3, bound=bound)
+        self.phases = [self.comp, self.lin]
+        self.dominant = self.lin
+        self.h2d_tensors = list(self.fts) + [self.x, self.ids]
+        self.d2h_tensors = [self.y] + [a for (_, a) in self.packed]
+        self.config = {"workload": f"grouped_14_variants_8192_{kind}", "variants": nv, "tokens": m,
+                       "ids": "uniform" if kind == "decode" else "zipf(1.1) segments, shuffled",
+                       "active_variants": active, "alpha": "scalar per variant",
+                       "l2": "inputs larger than L2 (14 W_ft of 128 MB each are compressed every step)"}
+
+    def oracle_sample(self, oracle, frac_rows: float):
+        c = self.cfg
+        n = max(8, int(c["n_out"] * frac_rows))
+        wb = synth.as_u16(self.w_base[:n])
+        fts = [synth.as_u16(wf[:n]) for wf in self.fts]
+        x = synth.as_u16(self.x)
+        modes = np.zeros(len(fts), np.int32)
+
+        def run():
+            bits, alphas = [], []
+            nbytes = 0.0
+            for wf in fts:
+                b, a, _ = oracle.compress(wb, wf, 0)
+                bits.append(b), alphas.append(a)
+                nbytes += 4.0 * wb.size + wb.size / 8
+            oracle.linear_grouped(x, self.ids_h, wb, bits, alphas, modes)
+            m = x.shape[0]
+            if self.metric_unit == "GB/s":
+                return nbytes + 2.0 * wb.size + len(fts) * wb.size / 8 + 2.0 * m * wb.shape[1] + 2.0 * m * n
+            return 2.0 * m * wb.size / 1e3
+        return run, f"first {frac_rows:.4g} of the rows: 14 compressions + the multi-tenant linear"
+
+
+WORKLOADS = {
+    "llama7b_layer_decode": lambda bd, dev: LayerWorkload(
+        bd, dev, workloads.LLAMA7B_LAYER, workloads.LLAMA7B_LAYER["ms"], "GB/s", "llama7b_layer_decode"),
+    "llama70b_linears_prefill": lambda bd, dev: LayerWorkload(
+        bd, dev, workloads.LLAMA70B_PREFILL, workloads.LLAMA70B_PREFILL["ms"], "TFLOP/s", "llama70b_linears_prefill",
+        private_io=False),
+    "grouped14_decode": lambda bd, dev: GroupedWorkload(bd, dev, "decode"),
+    "grouped14_prefill": lambda bd, dev: GroupedWorkload(bd, dev, "prefill"),
+    "llama3_8b_stack_decode": lambda bd, dev: LayerWorkload(
+        bd, dev, workloads.LLAMA3_8B_STACK, (1,), "GB/s", "llama3_8b_stack_decode",
+        layers=workloads.LLAMA3_8B_STACK["layers"], private_io=False),
+    "llama3_8b_stack_prefill": lambda bd, dev: LayerWorkload(
+        bd, dev, workloads.LLAMA3_8B_STACK, (2048,), "TFLOP/s", "llama3_8b_stack_prefill",
+        layers=workloads.LLAMA3_8B_STACK["layers"], private_io=False),
+}
 
 
 # --------------------------------------------------------------------------- arms
@@ -308,8 +422,7 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status after timing: {bd.bd_status_string(status)}")
 
     t_max = max_over_ranks(ws, total_ms)
-    step_bytes = wl.step_bytes()
-    value = ws * args.steps * step_bytes / (t_max * 1e-3) / 1e9
+    value = ws * args.steps * wl.step_work() / (t_max * 1e-3) / 1e9
 
     dom = wl.dominant
     dom_idx = wl.phases.index(dom)
@@ -320,6 +433,7 @@ def run_ours(args, ws, rank, local):
     else:
         achieved = dom.flops / dom.launches / dom_launch_s / 1e12
         peak, unit = peaks["bf16"], "TFLOP/s"
+    traffic = lookup_traffic(args.workload, dom)
     breakdown = {}
     for j, p in enumerate(wl.phases):
         t = phase_ms[j] * 1e-3 / args.steps
@@ -342,7 +456,8 @@ def run_ours(args, ws, rank, local):
         "dtype": "bf16", "data": "synthetic (seeded; N(0,sigma) bf16 base, Laplace deltas, N(0,1) activations)",
         "config": dict(wl.config, parallelism=f"replicas{ws}" if ws > 1 else "single"),
         "roofline": {"bound": dom.bound, "kernel": dom.name, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "peak_source": peaks["source"], "traffic": None},
+                     "frac": achieved / peak, "peak_source": peaks["source"], "traffic": traffic,
+                     **({"frac_of_sustained": achieved / peaks["bf16_sustained"]} if dom.bound == "tensor" else {})},
         "breakdown": breakdown,
         "e2e": e2e,
         "gpu_launches": args.steps * sum(p.launches for p in wl.phases),
@@ -351,6 +466,27 @@ def run_ours(args, ws, rank, local):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+KERNEL_SOURCES = {"hbm": "decode_tma.cu", "tensor": "prefill.cu"}
+
+
+def lookup_traffic(workload: str, phase):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    profiles/traffic_<workload>.md, if the kernel source is unchanged since the capture."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
+    src = os.path.join(ROOT, "bit_delta_tenant_gb300", "csrc", KERNEL_SOURCES[phase.bound])
+    try:
+        text = open(path).read()
+        digest = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)\s+source_sha1:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != digest:
+        return None
+    return float(m.group(1))
 
 
 def run_e2e(args, wl, stream, ws):
@@ -380,7 +516,7 @@ def run_e2e(args, wl, stream, ws):
         e.record(stream)
     torch.cuda.synchronize()
     t = max_over_ranks(ws, s.elapsed_time(e))
-    return {"value": ws * args.steps * wl.step_bytes() / (t * 1e-3) / 1e9, "unit": wl.metric_unit,
+    return {"value": ws * args.steps * wl.step_work() / (t * 1e-3) / 1e9, "unit": wl.metric_unit,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": t / args.steps}
 
 
@@ -417,7 +553,7 @@ def run_reference(args, ws, rank):
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     from bit_delta_tenant_gb300 import bitdelta as bd  # noqa: F401  (workload construction only)
     wl = WORKLOADS[args.workload](_NoLib(), dev)
-    frac = 1.0 / 16
+    frac = 1.0 / 64
     run, desc = wl.oracle_sample(oracle, frac)
     for _ in range(args.warmup):
         run()
@@ -441,6 +577,9 @@ class _NoLib:
     """Stands in for the library when only the workload's inputs are needed (reference arm)."""
 
     def bd_compress_workspace_size(self, *a):
+        return 16
+
+    def bd_linear_grouped_workspace_size(self, *a):
         return 16
 
     def __getattr__(self, name):
