@@ -87,6 +87,21 @@ cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *
                                    int64_t n_out, int64_t n_in, void *y, const GroupTable &tab, const DevCtx &ctx,
                                    cudaStream_t stream);
 
+// Tensor-core streaming multi-tenant kernel for small batches (grouped_decode_tc.cu).
+bool grouped_decode_tc_supported(int64_t m, int32_t n_variants, int64_t n_in, const void *x_sorted,
+                                 const void *w_base, const GroupedVariants &vars);
+cudaError_t launch_grouped_decode_tc(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
+                                     int64_t n_out, int64_t n_in, void *y, const int32_t *seg, const int32_t *perm,
+                                     const DevCtx &ctx, cudaStream_t stream);
+
+// mma.sync streaming multi-tenant kernel for small batches (grouped_decode.cu).
+bool grouped_decode_supported(int64_t m, int32_t n_variants, int64_t n_in, const void *w_base,
+                              const GroupedVariants &vars);
+cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
+                                  int64_t n_out, int64_t n_in, void *y, const int32_t *s_tiles,
+                                  const int32_t *n_s_tiles, const int32_t *perm, const int32_t *n_valid,
+                                  const DevCtx &ctx, cudaStream_t stream);
+
 size_t grouped_workspace_size(int64_t m, int32_t n_variants, int64_t n_out, int64_t n_in);
 cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const void *w_base,
                            const GroupedVariants &vars, int64_t n_out, int64_t n_in, void *y, void *ws,

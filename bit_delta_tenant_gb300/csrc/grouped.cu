@@ -11,14 +11,17 @@
 //   1. sort: a stable counting sort of the tokens by variant id (one block;
 //      each warp owns a contiguous token range, ranks equal ids within a
 //      32-token slice with __match_any_sync, and per-warp counts give every
-//      token its place), writing segment starts, the permutation, a
-//      padded-by-8 layout for the streaming kernel and the token-tile table
-//      for the tensor-core kernel.  Ids outside [0, V) set
+//      token its place), writing segment starts, the permutation and the
+//      tile tables of the two compute kernels.  Ids outside [0, V) set
 //      BD_ERR_BAD_VARIANT_ID in the status word and their tokens are skipped.
 //   2. gather: the activations in variant order (a plain row copy).
-//   3. compute: each variant's token segment runs against the shared W_base
-//      with its own bits and alpha; outputs go straight back to the original
-//      token rows.
+//   3. compute: small batches (m <= 64) run a streaming kernel that reads
+//      W_base and every variant's bits once (grouped_decode.cu on mma.sync; a
+//      tcgen05 variant, grouped_decode_tc.cu, is selectable); larger ones the
+//      tensor-core kernel over per-variant token tiles (prefill.cu).  Outputs go straight back to
+//      the original token rows.
+#include <cstdlib>
+
 #include "bd_device.cuh"
 #include "bd_internal.h"
 
@@ -28,34 +31,35 @@ namespace {
 constexpr int kSortThreads = 1024;
 constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kTileRows = 256;  // token rows per tensor-core tile
-constexpr int kPad = 8;         // padding granule of the streaming layout
+constexpr int kPad = 8;         // tokens per sign tile of the streaming kernel
+constexpr int kMaxSignTilesRead = 24;  // the streaming kernel reads this many table entries
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct WsLayout {
-    size_t seg, pseg, perm, pperm, tiles, n_tiles, xs, total;
-    int64_t padded_rows, max_slots;
+    size_t seg, perm, tiles, n_tiles, s_tiles, n_s_tiles, xs, total;
+    int64_t max_slots, max_s_tiles;
 };
 
 WsLayout layout(int64_t m, int32_t nv, int64_t n_in) {
     WsLayout L;
-    L.padded_rows = m + static_cast<int64_t>(kPad) * nv;
     L.max_slots = (m + kTileRows - 1) / kTileRows + nv;
+    L.max_s_tiles = (m + kPad - 1) / kPad + nv + kMaxSignTilesRead;  // room for the streaming kernel's fixed read
     size_t off = 0;
     L.seg = off;
     off = align256(off + sizeof(int32_t) * (nv + 1));
-    L.pseg = off;
-    off = align256(off + sizeof(int32_t) * (nv + 1));
     L.perm = off;
     off = align256(off + sizeof(int32_t) * static_cast<size_t>(m > 0 ? m : 1));
-    L.pperm = off;
-    off = align256(off + sizeof(int32_t) * static_cast<size_t>(L.padded_rows));
     L.tiles = off;
     off = align256(off + sizeof(int32_t) * 3 * static_cast<size_t>(L.max_slots));
     L.n_tiles = off;
     off = align256(off + sizeof(int32_t));
+    L.s_tiles = off;
+    off = align256(off + sizeof(int32_t) * 3 * static_cast<size_t>(L.max_s_tiles));
+    L.n_s_tiles = off;
+    off = align256(off + sizeof(int32_t));
     L.xs = off;
-    off = align256(off + 2 * static_cast<size_t>(L.padded_rows) * static_cast<size_t>(n_in));
+    off = align256(off + 2 * static_cast<size_t>(m > 0 ? m : 1) * static_cast<size_t>(n_in));
     L.total = off;
     return L;
 }
@@ -64,21 +68,18 @@ struct SortArgs {
     const int32_t *ids;
     int64_t m;
     int32_t nv;
-    int32_t *seg, *pseg, *perm, *pperm, *tiles, *n_tiles;
-    int64_t padded_rows;
+    int32_t *seg, *perm, *tiles, *n_tiles, *s_tiles, *n_s_tiles;
     unsigned *status;
 };
 
 __global__ void __launch_bounds__(kSortThreads, 1) group_sort_kernel(SortArgs a) {
     __shared__ int32_t cnt[kSortWarps][kMaxVariantsDev];  // per-warp counts, then running offsets
     __shared__ int32_t seg_s[kMaxVariantsDev + 1];
-    __shared__ int32_t pseg_s[kMaxVariantsDev + 1];
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int i = tid; i < kSortWarps * kMaxVariantsDev; i += kSortThreads) (&cnt[0][0])[i] = 0;
-    for (int64_t i = tid; i < a.padded_rows; i += kSortThreads) a.pperm[i] = -1;
     __syncthreads();
 
     // Contiguous per-warp token ranges, a multiple of 32 long.
@@ -105,20 +106,18 @@ __global__ void __launch_bounds__(kSortThreads, 1) group_sort_kernel(SortArgs a)
     if (bad) flag_status(a.status, kDevBadVariant);
     __syncthreads();
 
-    // Segment starts (compact and padded-by-8), per-warp offsets, tile table.
+    // Segment starts, per-warp offsets, and the two tile tables: up to 256
+    // tokens of one variant per tensor-core tile, up to 8 per streaming sign tile.
     if (tid == 0) {
-        int32_t s = 0, ps = 0;
+        int32_t s = 0;
         for (int v = 0; v < a.nv; ++v) {
             int32_t tot = 0;
             for (int w = 0; w < kSortWarps; ++w) tot += cnt[w][v];
             seg_s[v] = s;
-            pseg_s[v] = ps;
             s += tot;
-            ps += (tot + kPad - 1) / kPad * kPad;
         }
         seg_s[a.nv] = s;
-        pseg_s[a.nv] = ps;
-        int32_t nt = 0;
+        int32_t nt = 0, ns = 0;
         for (int v = 0; v < a.nv; ++v) {
             const int32_t len = seg_s[v + 1] - seg_s[v];
             for (int32_t j = 0; j < len; j += kTileRows) {
@@ -127,8 +126,15 @@ __global__ void __launch_bounds__(kSortThreads, 1) group_sort_kernel(SortArgs a)
                 a.tiles[3 * nt + 2] = min(kTileRows, len - j);
                 ++nt;
             }
+            for (int32_t j = 0; j < len; j += kPad) {
+                a.s_tiles[3 * ns] = v;
+                a.s_tiles[3 * ns + 1] = seg_s[v] + j;
+                a.s_tiles[3 * ns + 2] = min(kPad, len - j);
+                ++ns;
+            }
         }
         *a.n_tiles = nt;
+        *a.n_s_tiles = ns;
     }
     __syncthreads();
     if (tid < a.nv) {
@@ -139,10 +145,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) group_sort_kernel(SortArgs a)
             off += c;
         }
     }
-    for (int i = tid; i <= a.nv; i += kSortThreads) {
-        a.seg[i] = seg_s[i];
-        a.pseg[i] = pseg_s[i];
-    }
+    for (int i = tid; i <= a.nv; i += kSortThreads) a.seg[i] = seg_s[i];
     __syncthreads();
 
     // Pass 2: the same walk; rank among equal ids in the slice keeps the sort stable.
@@ -157,7 +160,6 @@ __global__ void __launch_bounds__(kSortThreads, 1) group_sort_kernel(SortArgs a)
         if (id >= 0) {
             const int32_t pos = cnt[warp][id] + __popc(peers & lt_mask);
             a.perm[pos] = static_cast<int32_t>(t);
-            a.pperm[pseg_s[id] + (pos - seg_s[id])] = static_cast<int32_t>(t);
         }
         __syncwarp();
         if (id >= 0 && (peers & lt_mask) == 0) cnt[warp][id] += __popc(peers);
@@ -198,12 +200,11 @@ cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const v
     s.m = m;
     s.nv = vars.count;
     s.seg = reinterpret_cast<int32_t *>(base + L.seg);
-    s.pseg = reinterpret_cast<int32_t *>(base + L.pseg);
     s.perm = reinterpret_cast<int32_t *>(base + L.perm);
-    s.pperm = reinterpret_cast<int32_t *>(base + L.pperm);
     s.tiles = reinterpret_cast<int32_t *>(base + L.tiles);
     s.n_tiles = reinterpret_cast<int32_t *>(base + L.n_tiles);
-    s.padded_rows = L.padded_rows;
+    s.s_tiles = reinterpret_cast<int32_t *>(base + L.s_tiles);
+    s.n_s_tiles = reinterpret_cast<int32_t *>(base + L.n_s_tiles);
     s.status = ctx.status;
     group_sort_kernel<<<1, kSortThreads, 0, stream>>>(s);
     cudaError_t e = cudaGetLastError();
@@ -221,6 +222,18 @@ cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const v
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
+    // Small batches: the mma.sync streaming kernel (fastest measured on GB300:
+    // the tcgen05 streaming kernel issues ~4 N=16 MMAs per variant and K block,
+    // each with an mbarrier round trip, and ends up latency-bound).
+    // BD_GROUPED_PATH=1/2/3 forces tcgen05 streaming / mma.sync streaming /
+    // per-variant tiles (tests and comparisons; unsupported shapes fall through).
+    const char *force = std::getenv("BD_GROUPED_PATH");
+    const int path = force ? std::atoi(force) : 0;
+    if (path == 1 && grouped_decode_tc_supported(m, vars.count, n_in, xs, w_base, vars))
+        return launch_grouped_decode_tc(xs, m, w_base, vars, n_out, n_in, y, s.seg, s.perm, ctx, stream);
+    if ((path == 0 || path == 1 || path == 2) && grouped_decode_supported(m, vars.count, n_in, w_base, vars))
+        return launch_grouped_decode(xs, m, w_base, vars, n_out, n_in, y, s.s_tiles, s.n_s_tiles, s.perm,
+                                     s.seg + vars.count, ctx, stream);
     GroupTable tab;
     tab.tiles = s.tiles;
     tab.n_tiles = s.n_tiles;

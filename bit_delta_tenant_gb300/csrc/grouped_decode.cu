@@ -1,0 +1,383 @@
+// grouped_decode.cu -- the multi-tenant fused linear for small batches (m <= 64
+// tokens, up to 16 variants): one HBM pass over the shared W_base and over
+// every variant's packed bits, fed by TMA.
+//
+// Method: "BitDelta : servir 14 modèles Zen depuis un seul cluster GPU"
+// (Hanzo blog), section "Architecture de service": the variants share one
+// resident W_base and each request's delta is applied on the fly, never
+// writing W_eff to HBM.
+//
+// Arithmetic (exact distributive form, fp32 alpha): for token t of variant v,
+//     y[t, j] = sum_k x[t,k] W_base[j,k]  +  alpha_v(j) * sum_k x[t,k] s^v_jk.
+// The base sum is one product over all tokens (in variant-sorted order, tiles
+// of 8 tokens); the sign sum runs per variant over 8-token tiles of that
+// variant's tokens, with the variant's signs built in registers (two integer
+// ops per pair); alpha, constant along k, multiplies the full fp32 sign sum.  Both run on
+// mma.m16n8k16 (W rows on the M side), like the single-variant streaming kernel.
+//
+// CTA: 8 consumer warps + 1 producer warp; 64 W rows.  A ring stage is a
+// 128-column K step: two 64x64 W boxes, two (tokens x 64) activation boxes
+// (128-byte swizzle) and one 64x16-byte packed-bit box per variant.  Warp w
+// owns row group w%4 and K half w/4; lane (g, t) reads 16-byte chunks 2t, 2t+1
+// of its rows and of the activation rows, so the MMA k-slots map to columns
+// 16t..16t+15 of the half.  A cluster of C CTAs splits K; partials are summed
+// across the halves in shared memory and across the cluster through
+// distributed shared memory, then written to the original token rows.
+#include <cooperative_groups.h>
+
+#include "bd_device.cuh"
+#include "bd_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace bd {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRows = 64;
+constexpr int kStepK = 128;
+constexpr int kMaxVar = 16;
+constexpr int kMaxS = 24;  // sign tiles of 8 tokens: m/8 + (variants present) <= 8 + 16
+constexpr uint32_t kBoxBytes = 64 * 64 * 2;
+constexpr uint32_t kBitsBox = kRows * 16;
+
+template <int NTB>
+struct GdRing {
+    static constexpr uint32_t kXBox = NTB * 1024;  // 8*NTB token rows x 128 bytes
+    static constexpr uint32_t kStageBytes = 2 * kBoxBytes + 2 * kXBox + kMaxVar * kBitsBox;
+    static constexpr int kStages = NTB >= 4 ? 4 : 5;
+    static constexpr uint32_t kRedBytes = 8 * NTB * kRows * 4;
+    static constexpr uint32_t kTableBytes = kMaxVar * kRows * 4 + 3 * kMaxS * 4 + 16;
+    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + kRedBytes + kTableBytes + 2 * kStages * 8 + 16;
+};
+
+struct GdMaps {
+    CUtensorMap w;
+    CUtensorMap x;
+    CUtensorMap b[kMaxVar];
+};
+
+struct GdArgs {
+    const float *alpha[kMaxVar];
+    int32_t mode[kMaxVar];
+    int32_t nv;
+    const int32_t *s_tiles;    // [kMaxS][3]: variant, first sorted row, rows (<= 8)
+    const int32_t *n_s_tiles;
+    const int32_t *perm;       // sorted row -> original token
+    const int32_t *n_valid;    // tokens with a valid id
+    uint16_t *y;
+    int64_t m, n_out, n_in, ks;
+    int32_t cluster;
+    unsigned *status;
+    uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+__device__ __forceinline__ void signs8(uint32_t two_bytes, uint32_t (&s)[8]) {
+    const uint32_t b0 = two_bytes & 0xFFu, b1 = (two_bytes >> 8) & 0xFFu;
+    s[0] = sign_pair_bf16<0>(b0), s[1] = sign_pair_bf16<1>(b0), s[2] = sign_pair_bf16<2>(b0);
+    s[3] = sign_pair_bf16<3>(b0), s[4] = sign_pair_bf16<0>(b1), s[5] = sign_pair_bf16<1>(b1);
+    s[6] = sign_pair_bf16<2>(b1), s[7] = sign_pair_bf16<3>(b1);
+}
+
+template <int NTB>
+__global__ void __launch_bounds__(kThreads, 1)
+    gdecode_kernel(const __grid_constant__ GdMaps maps, const __grid_constant__ GdArgs a) {
+    using R = GdRing<NTB>;
+    constexpr int MP = 8 * NTB;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *red = reinterpret_cast<float *>(smem + R::kStages * R::kStageBytes);
+    float *alpha_s = red + R::kRedBytes / 4;                       // [kMaxVar][kRows]
+    int32_t *tiles_s = reinterpret_cast<int32_t *>(alpha_s + kMaxVar * kRows);  // [kMaxS][3]
+    int32_t *n_tiles_s = tiles_s + 3 * kMaxS;
+    uint64_t *full = reinterpret_cast<uint64_t *>(
+        smem + R::kStages * R::kStageBytes + R::kRedBytes + R::kTableBytes);
+    uint64_t *empty = full + R::kStages;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + R::kStages);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int64_t row_block = blockIdx.x / a.cluster;
+    const int row0 = static_cast<int>(row_block * kRows);
+    const int64_t k_lo = static_cast<int64_t>(rank) * a.ks;
+    const int64_t k_hi = min(k_lo + a.ks, a.n_in);
+    const int n_steps = k_hi > k_lo ? static_cast<int>((k_hi - k_lo + kStepK - 1) / kStepK) : 0;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < R::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_trigger_and_wait();
+    // Per-variant alpha of this CTA's rows and the sign-tile table, in shared memory.
+    for (int i = threadIdx.x; i < a.nv * kRows; i += kThreads) {
+        const int v = i / kRows, r = i - v * kRows;
+        const int64_t row = static_cast<int64_t>(row0) + r;
+        alpha_s[i] = row < a.n_out ? (a.mode[v] ? a.alpha[v][row] : a.alpha[v][0]) : 0.0f;
+    }
+    if (threadIdx.x < 3 * kMaxS) tiles_s[threadIdx.x] = a.s_tiles[threadIdx.x];
+    if (threadIdx.x == 0) *n_tiles_s = min(*a.n_s_tiles, kMaxS);
+    __syncthreads();
+    const int n_st = *n_tiles_s;
+
+    const int g = lane >> 2, t = lane & 3;
+    const int rg = warp & 3, kh = warp >> 2;
+    const int r0 = rg * 16 + g;
+
+    float accb[NTB][4], accs[kMaxS][4];
+#pragma unroll
+    for (int i = 0; i < NTB; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) accb[i][j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxS; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) accs[i][j] = 0.0f;
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.w);
+            tma_prefetch_desc(&maps.x);
+            const uint32_t tx = 2 * kBoxBytes + 2 * R::kXBox + a.nv * kBitsBox;
+            int issued = 0;
+            for (int i = 0; i < n_steps; ++i) {
+                const int s = i % R::kStages;
+                if (!mbar_wait(&empty[s], ((i / R::kStages) & 1) ^ 1, a.wait_ns, abort_flag)) {
+                    *abort_flag = 1;
+                    flag_status(a.status, kDevTimeout);
+                    break;
+                }
+                const int kc = static_cast<int>(k_lo) + i * kStepK;
+                uint8_t *st = smem + s * R::kStageBytes;
+                mbar_arrive_expect_tx(&full[s], tx);
+                tma_load_2d(st, &maps.w, &full[s], kc, row0);
+                tma_load_2d(st + kBoxBytes, &maps.w, &full[s], kc + 64, row0);
+                tma_load_2d(st + 2 * kBoxBytes, &maps.x, &full[s], kc, 0);
+                tma_load_2d(st + 2 * kBoxBytes + R::kXBox, &maps.x, &full[s], kc + 64, 0);
+                for (int v = 0; v < a.nv; ++v)
+                    tma_load_2d(st + 2 * kBoxBytes + 2 * R::kXBox + v * kBitsBox, &maps.b[v], &full[s], kc / 8, row0);
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                for (int i = (issued > R::kStages ? issued - R::kStages : 0); i < issued; ++i)
+                    mbar_wait(&full[i % R::kStages], (i / R::kStages) & 1, kDrainLimitNs, nullptr);
+            }
+        }
+    } else {
+        const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ g) << 4);      // rows with (row & 7) == g
+        const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ g) << 4);
+        for (int i = 0; i < n_steps; ++i) {
+            const int s = i % R::kStages;
+            const bool got = mbar_wait(&full[s], (i / R::kStages) & 1, a.wait_ns, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    flag_status(a.status, kDevTimeout);
+                }
+                break;
+            }
+            const uint8_t *st = smem + s * R::kStageBytes;
+            const uint8_t *box = st + kh * kBoxBytes;
+            const uint4 wa0 = lds128(box + r0 * 128 + sw0), wa1 = lds128(box + r0 * 128 + sw1);
+            const uint4 wb0 = lds128(box + (r0 + 8) * 128 + sw0), wb1 = lds128(box + (r0 + 8) * 128 + sw1);
+            const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
+            const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+            const uint8_t *xbox = st + 2 * kBoxBytes + kh * R::kXBox;
+            const uint8_t *bits = st + 2 * kBoxBytes + 2 * R::kXBox + kh * 8 + 2 * t;
+
+            // base: every token (sorted order), 8 per tile
+#pragma unroll
+            for (int tt = 0; tt < NTB; ++tt) {
+                const uint4 p0 = lds128(xbox + (8 * tt + g) * 128 + sw0);
+                const uint4 p1 = lds128(xbox + (8 * tt + g) * 128 + sw1);
+                const uint32_t xv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    mma_bf16_16816(accb[tt], wa[2 * j], wb[2 * j], wa[2 * j + 1], wb[2 * j + 1], xv[2 * j],
+                                   xv[2 * j + 1]);
+            }
+            // signs: each tile holds up to 8 tokens of one variant
+#pragma unroll
+            for (int q = 0; q < kMaxS; ++q) {
+                if (q < n_st) {
+                    const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
+                    uint32_t sa[8], sb[8];
+                    signs8(*reinterpret_cast<const uint16_t *>(bits + v * kBitsBox + r0 * 16), sa);
+                    signs8(*reinterpret_cast<const uint16_t *>(bits + v * kBitsBox + (r0 + 8) * 16), sb);
+                    const int xr = start + g;
+                    uint4 p0 = make_uint4(0, 0, 0, 0), p1 = make_uint4(0, 0, 0, 0);
+                    if (g < cnt) {
+                        const uint32_t c0 = static_cast<uint32_t>(((2 * t) ^ (xr & 7)) << 4);
+                        const uint32_t c1 = static_cast<uint32_t>(((2 * t + 1) ^ (xr & 7)) << 4);
+                        p0 = lds128(xbox + xr * 128 + c0);
+                        p1 = lds128(xbox + xr * 128 + c1);
+                    }
+                    const uint32_t xv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_bf16_16816(accs[q], sa[2 * j], sb[2 * j], sa[2 * j + 1], sb[2 * j + 1], xv[2 * j],
+                                       xv[2 * j + 1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        // ---- red[sorted token][row]: base then signs, both K halves, in a fixed order ----
+        auto put_base = [&](bool add) {
+#pragma unroll
+            for (int tt = 0; tt < NTB; ++tt) {
+                const int c = 8 * tt + 2 * t;
+                float *p = red + c * kRows + r0;
+                if (add) {
+                    p[0] += accb[tt][0], p[kRows] += accb[tt][1], p[8] += accb[tt][2], p[kRows + 8] += accb[tt][3];
+                } else {
+                    p[0] = accb[tt][0], p[kRows] = accb[tt][1], p[8] = accb[tt][2], p[kRows + 8] = accb[tt][3];
+                }
+            }
+        };
+        auto add_signs = [&]() {  // alpha is constant along k: applied once to the full sign sums
+#pragma unroll
+            for (int q = 0; q < kMaxS; ++q) {
+                if (q < n_st) {
+                    const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
+                    const float al0 = alpha_s[v * kRows + r0], al1 = alpha_s[v * kRows + r0 + 8];
+                    if (2 * t < cnt) {
+                        float *p = red + (start + 2 * t) * kRows + r0;
+                        p[0] += al0 * accs[q][0];
+                        p[8] += al1 * accs[q][2];
+                    }
+                    if (2 * t + 1 < cnt) {
+                        float *p = red + (start + 2 * t + 1) * kRows + r0;
+                        p[0] += al0 * accs[q][1];
+                        p[8] += al1 * accs[q][3];
+                    }
+                }
+            }
+        };
+        if (kh == 1) put_base(false);
+        consumer_sync();
+        if (kh == 0) put_base(true);
+        consumer_sync();
+        if (kh == 1) add_signs();
+        consumer_sync();
+        if (kh == 0) add_signs();
+    }
+    cluster.sync();
+
+    // ---- rank c sums rows [c*share, (c+1)*share) over the cluster; scatter to original tokens ----
+    const int share = (kRows + a.cluster - 1) / a.cluster;
+    const int n_tok = min(*a.n_valid, MP);
+    for (int i = threadIdx.x; i < share * n_tok; i += kThreads) {
+        const int tok = i / share;
+        const int lr = rank * share + (i - tok * share);
+        const int64_t row = static_cast<int64_t>(row0) + lr;
+        if (lr < kRows && row < a.n_out) {
+            float s = 0.0f;
+            for (int q = 0; q < a.cluster; ++q) s += cluster.map_shared_rank(red, q)[tok * kRows + lr];
+            __nv_bfloat16 h = __float2bfloat16_rn(s);
+            a.y[static_cast<int64_t>(a.perm[tok]) * a.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
+        }
+    }
+    cluster.sync();
+}
+
+template <int NTB>
+cudaError_t launch_ntb(const GdMaps &maps, const GdArgs &a, int64_t row_blocks, const DevCtx &ctx,
+                       cudaStream_t stream) {
+    static bool attr_set[128] = {false};
+    if (ctx.device < 128 && !attr_set[ctx.device]) {
+        cudaError_t e = cudaFuncSetAttribute(gdecode_kernel<NTB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(GdRing<NTB>::kSmem));
+        if (e != cudaSuccess) return e;
+        attr_set[ctx.device] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(row_blocks * a.cluster), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = GdRing<NTB>::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gdecode_kernel<NTB>, maps, a);
+}
+
+}  // namespace
+
+bool grouped_decode_supported(int64_t m, int32_t n_variants, int64_t n_in, const void *w_base,
+                              const GroupedVariants &vars) {
+    if (m < 1 || m > 64 || n_variants > kMaxVar || n_in % kStepK != 0) return false;
+    if (m / 8 + (m < n_variants ? m : n_variants) + 1 > kMaxS) return false;
+    if (reinterpret_cast<uintptr_t>(w_base) & 15) return false;
+    for (int v = 0; v < vars.count; ++v)
+        if (reinterpret_cast<uintptr_t>(vars.bits[v]) & 15) return false;
+    return true;
+}
+
+cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
+                                  int64_t n_out, int64_t n_in, void *y, const int32_t *s_tiles,
+                                  const int32_t *n_s_tiles, const int32_t *perm, const int32_t *n_valid,
+                                  const DevCtx &ctx, cudaStream_t stream) {
+    const int ntb = m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8;
+    GdMaps maps;
+    if (!encode_tensor_map_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, 64, kRows,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_tensor_map_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_sorted, n_in, m, n_in * 2, 64,
+                              static_cast<uint32_t>(8 * ntb), CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    GdArgs a = {};
+    for (int v = 0; v < vars.count; ++v) {
+        if (!encode_tensor_map_2d(&maps.b[v], CU_TENSOR_MAP_DATA_TYPE_UINT8, vars.bits[v], n_in / 8, n_out, n_in / 8,
+                                  16, kRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        a.alpha[v] = vars.alpha[v];
+        a.mode[v] = vars.mode[v];
+    }
+    a.nv = vars.count;
+    a.s_tiles = s_tiles;
+    a.n_s_tiles = n_s_tiles;
+    a.perm = perm;
+    a.n_valid = n_valid;
+    a.y = static_cast<uint16_t *>(y);
+    a.m = m;
+    a.n_out = n_out;
+    a.n_in = n_in;
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
+    // K split over a cluster when the 64-row blocks leave SMs idle (one CTA per SM here).
+    const int64_t row_blocks = (n_out + kRows - 1) / kRows;
+    const int64_t steps = n_in / kStepK;
+    int64_t c = row_blocks >= ctx.num_sms ? 1 : (ctx.num_sms + row_blocks - 1) / row_blocks;
+    if (c > 8) c = 8;
+    if (c > steps) c = steps;
+    const int64_t per = (steps + c - 1) / c;
+    a.ks = per * kStepK;
+    a.cluster = static_cast<int32_t>((steps + per - 1) / per);
+    if (row_blocks * a.cluster > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    switch (ntb) {
+        case 1: return launch_ntb<1>(maps, a, row_blocks, ctx, stream);
+        case 2: return launch_ntb<2>(maps, a, row_blocks, ctx, stream);
+        case 4: return launch_ntb<4>(maps, a, row_blocks, ctx, stream);
+        default: return launch_ntb<8>(maps, a, row_blocks, ctx, stream);
+    }
+}
+
+}  // namespace bd

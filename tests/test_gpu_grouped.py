@@ -127,7 +127,7 @@ def test_out_of_range_id_is_reported_and_other_tokens_are_correct():
 
 
 @pytest.mark.parametrize("kind", ["decode", "prefill"])
-def test_fourteen_variant_workload_full_size(kind):
+def test_fourteen_variant_workload_full_size(kind, grouped_path):
     c = workloads.GROUPED_14
     m = c["decode_m"] if kind == "decode" else c["prefill_m"]
     ids = synth.uniform_ids(m, c["n_variants"], c["seed"]) if kind == "decode" else \
@@ -141,3 +141,32 @@ def test_fourteen_variant_workload_full_size(kind):
     ts, js = sample_outputs(case.m, case.n_out, 1500, seed=m)
     y_ref, mag = case.reference_sampled(ts, js)
     assert_y_close(yh[ts, js], y_ref, mag, f"14-variant {kind}")
+
+
+@pytest.fixture(params=["1", "2", "3"], ids=["tcgen05_stream", "mma_stream", "per_variant_tiles"])
+def grouped_path(request, monkeypatch):
+    """Force one multi-tenant kernel (shapes a kernel cannot take fall through to the next)."""
+    monkeypatch.setenv("BD_GROUPED_PATH", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("n_out,n_in,m,n_var", [(129, 256, 64, 14), (64, 1152, 1, 3), (300, 128, 33, 16),
+                                                 (1000, 4096, 9, 5), (65, 640, 64, 12), (7, 384, 17, 2),
+                                                 (200, 192, 40, 7), (513, 2048, 64, 14)])
+def test_streaming_kernel_shapes_and_mixed_modes(n_out, n_in, m, n_var, grouped_path):
+    """Small batches: every kernel against the oracle, ragged rows, mixed alpha modes."""
+    ids = synth.uniform_ids(m, n_var, seed=n_out + m)
+    modes = [v % 2 for v in range(n_var)]
+    case = GroupedCase(n_out, n_in, n_var, ids, modes=modes, seed=n_in + m)
+    check_full(case, f"grouped path={grouped_path} {n_out}x{n_in} m={m} V={n_var}")
+
+
+def test_streaming_kernel_bad_id_and_empty_variants(grouped_path):
+    ids = np.array([0, 5, 2, 2, 9, -3, 0, 2, 5, 5, 5], np.int32)  # variants 1, 3, 4 empty; 9 and -3 invalid
+    case = GroupedCase(256, 512, 6, ids, modes=[1, 0, 1, 0, 1, 0], seed=12)
+    y = case.run()
+    assert bd.bd_get_device_status() == bd.BD_ERR_BAD_VARIANT_ID
+    good = np.where((ids >= 0) & (ids < 6))[0]
+    y_ref, mag = oracle.linear_grouped(case.x_h[good], ids[good], case.wb_h, case.bits_h, case.alpha_h,
+                                       np.array(case.modes, np.int32))
+    assert_y_close(y_host(y)[good], y_ref, mag, "good tokens (streaming)")
