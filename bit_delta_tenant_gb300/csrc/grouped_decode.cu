@@ -15,14 +15,15 @@
 // ops per pair); alpha, constant along k, multiplies the full fp32 sign sum.  Both run on
 // mma.m16n8k16 (W rows on the M side), like the single-variant streaming kernel.
 //
-// CTA: 8 consumer warps + 1 producer warp; 64 W rows.  A ring stage is a
+// CTA: 16 consumer warps + 1 TMA producer warp; 64 W rows.  A ring stage is a
 // 128-column K step: two 64x64 W boxes, two (tokens x 64) activation boxes
-// (128-byte swizzle) and one 64x16-byte packed-bit box per variant.  Warp w
-// owns row group w%4 and K half w/4; lane (g, t) reads 16-byte chunks 2t, 2t+1
+// (128-byte swizzle) and one 64x16-byte packed-bit box per variant.  Consumer
+// warp w owns row group w%4 and every fourth token tile (w/4) over both K
+// halves, processing its sign tiles in interleaved pairs; lane (g, t) reads 16-byte chunks 2t, 2t+1
 // of its rows and of the activation rows, so the MMA k-slots map to columns
-// 16t..16t+15 of the half.  A cluster of C CTAs splits K; partials are summed
-// across the halves in shared memory and across the cluster through
-// distributed shared memory, then written to the original token rows.
+// 16t..16t+15 of the half.  A cluster of C CTAs splits K; each token's base
+// and sign parts meet in shared memory and the cluster's K slices are summed
+// through distributed shared memory, then written to the original token rows.
 #include <cooperative_groups.h>
 
 #include "bd_device.cuh"
@@ -33,8 +34,8 @@ namespace cg = cooperative_groups;
 namespace bd {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerWarps = 16;  // 4 row groups x 4 token-tile quarters
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + the TMA producer warp
 constexpr int kRows = 64;
 constexpr int kStepK = 128;
 constexpr int kMaxVar = 16;
@@ -73,7 +74,6 @@ struct GdArgs {
     uint64_t wait_ns;
 };
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
 __device__ __forceinline__ void signs8(uint32_t two_bytes, uint32_t (&s)[8]) {
@@ -125,26 +125,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t row = static_cast<int64_t>(row0) + r;
         alpha_s[i] = row < a.n_out ? (a.mode[v] ? a.alpha[v][row] : a.alpha[v][0]) : 0.0f;
     }
-    if (threadIdx.x < 3 * kMaxS) tiles_s[threadIdx.x] = a.s_tiles[threadIdx.x];
-    if (threadIdx.x == 0) *n_tiles_s = min(*a.n_s_tiles, kMaxS);
+    {
+        const int n_valid_tiles = min(*a.n_s_tiles, kMaxS);
+        // entries past the last tile become empty tiles (no tokens) so pairs need no branch
+        if (threadIdx.x < 3 * kMaxS) tiles_s[threadIdx.x] = threadIdx.x < 3 * n_valid_tiles ? a.s_tiles[threadIdx.x] : 0;
+        if (threadIdx.x == 0) *n_tiles_s = n_valid_tiles;
+    }
     __syncthreads();
     const int n_st = *n_tiles_s;
 
     const int g = lane >> 2, t = lane & 3;
-    const int rg = warp & 3, kh = warp >> 2;
+    const int rg = warp & 3, tq = warp >> 2;  // row group, token-tile quarter
     const int r0 = rg * 16 + g;
+    constexpr int NB = (NTB + 3) / 4;       // base tiles tt = 4i + tq
+    constexpr int NS = kMaxS / 4;           // sign tiles q = 4i + tq
 
-    float accb[NTB][4], accs[kMaxS][4];
+    float accb[NB][4], accs[NS][4];
 #pragma unroll
-    for (int i = 0; i < NTB; ++i)
+    for (int i = 0; i < NB; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) accb[i][j] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kMaxS; ++i)
+    for (int i = 0; i < NS; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) accs[i][j] = 0.0f;
 
     if (warp == kConsumerWarps) {
+        // ---- TMA producer ----
         if (lane == 0) {
             tma_prefetch_desc(&maps.w);
             tma_prefetch_desc(&maps.x);
@@ -168,111 +175,125 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(st + 2 * kBoxBytes + 2 * R::kXBox + v * kBitsBox, &maps.b[v], &full[s], kc / 8, row0);
                 issued = i + 1;
             }
-            if (*abort_flag) {
+            if (*abort_flag) {  // drain this CTA's copies still in flight
                 for (int i = (issued > R::kStages ? issued - R::kStages : 0); i < issued; ++i)
                     mbar_wait(&full[i % R::kStages], (i / R::kStages) & 1, kDrainLimitNs, nullptr);
             }
         }
     } else {
-        const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ g) << 4);      // rows with (row & 7) == g
-        const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ g) << 4);
-        for (int i = 0; i < n_steps; ++i) {
-            const int s = i % R::kStages;
-            const bool got = mbar_wait(&full[s], (i / R::kStages) & 1, a.wait_ns, abort_flag);
-            if (!__all_sync(0xFFFFFFFFu, got)) {
-                if (lane == 0) {
-                    *abort_flag = 1;
-                    flag_status(a.status, kDevTimeout);
-                }
-                break;
+    // Constants of this warp's sign tiles q = 4i + tq (the same in every K step).
+    const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ g) << 4);      // rows with (row & 7) == g
+    const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ g) << 4);
+    const int n_mine = n_st > tq ? (n_st - tq + 3) / 4 : 0;
+    const int n_pairs = (n_mine + 1) / 2;
+    int x_off[NS], b_off[NS];  // x_off < 0: this lane's token row is past the tile
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int q = 4 * i + tq;
+        const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
+        const int xr = start + g;
+        x_off[i] = g < cnt ? xr * 128 + (((2 * t) ^ (xr & 7)) << 4) : -1;
+        b_off[i] = v * kBitsBox + r0 * 16 + 2 * t;
+    }
+
+    bool ok = true;
+    for (int i = 0; i < n_steps; ++i) {
+        const int s = i % R::kStages;
+        const bool got = mbar_wait(&full[s], (i / R::kStages) & 1, a.wait_ns, abort_flag);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                flag_status(a.status, kDevTimeout);
             }
-            const uint8_t *st = smem + s * R::kStageBytes;
+            ok = false;
+            break;
+        }
+        const uint8_t *st = smem + s * R::kStageBytes;
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) {
             const uint8_t *box = st + kh * kBoxBytes;
             const uint4 wa0 = lds128(box + r0 * 128 + sw0), wa1 = lds128(box + r0 * 128 + sw1);
             const uint4 wb0 = lds128(box + (r0 + 8) * 128 + sw0), wb1 = lds128(box + (r0 + 8) * 128 + sw1);
             const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
             const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
             const uint8_t *xbox = st + 2 * kBoxBytes + kh * R::kXBox;
-            const uint8_t *bits = st + 2 * kBoxBytes + 2 * R::kXBox + kh * 8 + 2 * t;
-
-            // base: every token (sorted order), 8 per tile
+            const uint8_t *bits = st + 2 * kBoxBytes + 2 * R::kXBox + kh * 8;
+            // base: this warp's 8-token tiles of all tokens (sorted order)
 #pragma unroll
-            for (int tt = 0; tt < NTB; ++tt) {
-                const uint4 p0 = lds128(xbox + (8 * tt + g) * 128 + sw0);
-                const uint4 p1 = lds128(xbox + (8 * tt + g) * 128 + sw1);
-                const uint32_t xv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mma_bf16_16816(accb[tt], wa[2 * j], wb[2 * j], wa[2 * j + 1], wb[2 * j + 1], xv[2 * j],
-                                   xv[2 * j + 1]);
-            }
-            // signs: each tile holds up to 8 tokens of one variant
-#pragma unroll
-            for (int q = 0; q < kMaxS; ++q) {
-                if (q < n_st) {
-                    const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
-                    uint32_t sa[8], sb[8];
-                    signs8(*reinterpret_cast<const uint16_t *>(bits + v * kBitsBox + r0 * 16), sa);
-                    signs8(*reinterpret_cast<const uint16_t *>(bits + v * kBitsBox + (r0 + 8) * 16), sb);
-                    const int xr = start + g;
-                    uint4 p0 = make_uint4(0, 0, 0, 0), p1 = make_uint4(0, 0, 0, 0);
-                    if (g < cnt) {
-                        const uint32_t c0 = static_cast<uint32_t>(((2 * t) ^ (xr & 7)) << 4);
-                        const uint32_t c1 = static_cast<uint32_t>(((2 * t + 1) ^ (xr & 7)) << 4);
-                        p0 = lds128(xbox + xr * 128 + c0);
-                        p1 = lds128(xbox + xr * 128 + c1);
-                    }
+            for (int ib = 0; ib < NB; ++ib) {
+                const int tt = 4 * ib + tq;
+                if (tt < NTB) {
+                    const uint4 p0 = lds128(xbox + (8 * tt + g) * 128 + sw0);
+                    const uint4 p1 = lds128(xbox + (8 * tt + g) * 128 + sw1);
                     const uint32_t xv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        mma_bf16_16816(accs[q], sa[2 * j], sb[2 * j], sa[2 * j + 1], sb[2 * j + 1], xv[2 * j],
+                        mma_bf16_16816(accb[ib], wa[2 * j], wb[2 * j], wa[2 * j + 1], wb[2 * j + 1], xv[2 * j],
                                        xv[2 * j + 1]);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            // signs: this warp's tiles in interleaved pairs (a missing second tile is empty)
+#pragma unroll
+            for (int ip = 0; ip < (NS + 1) / 2; ++ip) {
+                if (ip < n_pairs) {
+                    uint32_t sa[2][8], sb[2][8], xv[2][8];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int i2 = 2 * ip + e < NS ? 2 * ip + e : NS - 1;
+                        signs8(*reinterpret_cast<const uint16_t *>(bits + b_off[i2]), sa[e]);
+                        signs8(*reinterpret_cast<const uint16_t *>(bits + b_off[i2] + 128), sb[e]);  // row r0 + 8
+                        uint4 p0 = make_uint4(0, 0, 0, 0), p1 = make_uint4(0, 0, 0, 0);
+                        if (x_off[i2] >= 0) {
+                            p0 = lds128(xbox + x_off[i2]);
+                            p1 = lds128(xbox + (x_off[i2] ^ 16));  // chunk 2t+1: flip the chunk's low bit
+                        }
+                        xv[e][0] = p0.x, xv[e][1] = p0.y, xv[e][2] = p0.z, xv[e][3] = p0.w;
+                        xv[e][4] = p1.x, xv[e][5] = p1.y, xv[e][6] = p1.z, xv[e][7] = p1.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            if (2 * ip + e < NS)
+                                mma_bf16_16816(accs[2 * ip + e], sa[e][2 * j], sb[e][2 * j], sa[e][2 * j + 1],
+                                               sb[e][2 * j + 1], xv[e][2 * j], xv[e][2 * j + 1]);
+                }
+            }
         }
-
-        // ---- red[sorted token][row]: base then signs, both K halves, in a fixed order ----
-        auto put_base = [&](bool add) {
-#pragma unroll
-            for (int tt = 0; tt < NTB; ++tt) {
-                const int c = 8 * tt + 2 * t;
-                float *p = red + c * kRows + r0;
-                if (add) {
-                    p[0] += accb[tt][0], p[kRows] += accb[tt][1], p[8] += accb[tt][2], p[kRows + 8] += accb[tt][3];
-                } else {
-                    p[0] = accb[tt][0], p[kRows] = accb[tt][1], p[8] = accb[tt][2], p[kRows + 8] = accb[tt][3];
-                }
-            }
-        };
-        auto add_signs = [&]() {  // alpha is constant along k: applied once to the full sign sums
-#pragma unroll
-            for (int q = 0; q < kMaxS; ++q) {
-                if (q < n_st) {
-                    const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
-                    const float al0 = alpha_s[v * kRows + r0], al1 = alpha_s[v * kRows + r0 + 8];
-                    if (2 * t < cnt) {
-                        float *p = red + (start + 2 * t) * kRows + r0;
-                        p[0] += al0 * accs[q][0];
-                        p[8] += al1 * accs[q][2];
-                    }
-                    if (2 * t + 1 < cnt) {
-                        float *p = red + (start + 2 * t + 1) * kRows + r0;
-                        p[0] += al0 * accs[q][1];
-                        p[8] += al1 * accs[q][3];
-                    }
-                }
-            }
-        };
-        if (kh == 1) put_base(false);
-        consumer_sync();
-        if (kh == 0) put_base(true);
-        consumer_sync();
-        if (kh == 1) add_signs();
-        consumer_sync();
-        if (kh == 0) add_signs();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
+    (void)ok;
+
+    // ---- red[sorted token][row] = base + alpha * signs (each token in one base and one sign tile) ----
+#pragma unroll
+    for (int ib = 0; ib < NB; ++ib) {
+        const int tt = 4 * ib + tq;
+        if (tt < NTB) {
+            float *p = red + (8 * tt + 2 * t) * kRows + r0;
+            p[0] = accb[ib][0], p[kRows] = accb[ib][1], p[8] = accb[ib][2], p[kRows + 8] = accb[ib][3];
+        }
+    }
+    asm volatile("bar.sync 1, 512;" ::: "memory");  // consumer warps only
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {  // alpha is constant along k: applied once to the full sign sums
+        const int q = 4 * i + tq;
+        if (q < n_st) {
+            const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
+            const float al0 = alpha_s[v * kRows + r0], al1 = alpha_s[v * kRows + r0 + 8];
+            if (2 * t < cnt) {
+                float *p = red + (start + 2 * t) * kRows + r0;
+                p[0] += al0 * accs[i][0];
+                p[8] += al1 * accs[i][2];
+            }
+            if (2 * t + 1 < cnt) {
+                float *p = red + (start + 2 * t + 1) * kRows + r0;
+                p[0] += al0 * accs[i][1];
+                p[8] += al1 * accs[i][3];
+            }
+        }
+    }
+    }  // consumers
     cluster.sync();
 
     // ---- rank c sums rows [c*share, (c+1)*share) over the cluster; scatter to original tokens ----
