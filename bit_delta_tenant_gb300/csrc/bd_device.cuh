@@ -72,6 +72,47 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait until the phase with parity `parity` of `bar` has completed, for at
 // most `limit_ns` of wall-clock time.  Gives up early if `*abort` becomes
 // non-zero (another role of the same CTA gave up).  Returns false on give-up.
+// Non-blocking probe of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps (issuing nothing) until the phase completes or about `hint_ns` pass.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait that sleeps between polls (for a warp that has nothing else
+// to do: a producer waiting for a free slot).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                                volatile int *abort, uint32_t hint_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (limit_ns == 0) return false;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
+        if (abort != nullptr && *abort != 0) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                           volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -15,7 +15,7 @@
 // ops per pair); alpha, constant along k, multiplies the full fp32 sign sum.  Both run on
 // mma.m16n8k16 (W rows on the M side), like the single-variant streaming kernel.
 //
-// CTA: 16 consumer warps + 1 TMA producer warp; 64 W rows.  A ring stage is a
+// CTA: 16 warps, each also issuing part of the TMA; 64 W rows.  A ring stage is a
 // 128-column K step: two 64x64 W boxes, two (tokens x 64) activation boxes
 // (128-byte swizzle) and one 64x16-byte packed-bit box per variant.  Consumer
 // warp w owns row group w%4 and every fourth token tile (w/4) over both K
@@ -35,7 +35,7 @@ namespace bd {
 namespace {
 
 constexpr int kConsumerWarps = 16;  // 4 row groups x 4 token-tile quarters
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + the TMA producer warp
+constexpr int kThreads = kConsumerWarps * 32;  // lane 0 of every warp also issues TMA boxes
 constexpr int kRows = 64;
 constexpr int kStepK = 128;
 constexpr int kMaxVar = 16;
@@ -72,15 +72,29 @@ struct GdArgs {
     int32_t cluster;
     unsigned *status;
     uint64_t wait_ns;
+    uint32_t sign_mul[4];      // 2^(15-2I) + 2^(30-2I), I = 0..3
 };
 
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
-__device__ __forceinline__ void signs8(uint32_t two_bytes, uint32_t (&s)[8]) {
-    const uint32_t b0 = two_bytes & 0xFFu, b1 = (two_bytes >> 8) & 0xFFu;
-    s[0] = sign_pair_bf16<0>(b0), s[1] = sign_pair_bf16<1>(b0), s[2] = sign_pair_bf16<2>(b0);
-    s[3] = sign_pair_bf16<3>(b0), s[4] = sign_pair_bf16<0>(b1), s[5] = sign_pair_bf16<1>(b1);
-    s[6] = sign_pair_bf16<2>(b1), s[7] = sign_pair_bf16<3>(b1);
+// Sign pairs of 16 packed bits read as two bytes (byte loads zero-extend for
+// free).  Pair I of a byte is ((byte * mul_I) & 0x80008000) ^ 0xBF80BF80 with
+// mul_I = 2^(15-2I) + 2^(30-2I) (the two shifted copies never overlap).  The
+// multipliers arrive as kernel parameters: a literal constant lets the
+// compiler turn the product into shifts and adds on the integer ALU, which
+// the sign expansion already saturates; a runtime multiplier keeps it a
+// single multiply-add on the FMA pipe.
+__device__ __forceinline__ uint32_t sign_pair_mul(uint32_t byte, uint32_t mul) {
+    return ((byte * mul) & 0x80008000u) ^ 0xBF80BF80u;
+}
+
+__device__ __forceinline__ void signs8(const uint8_t *p, const uint32_t (&mul)[4], uint32_t (&s)[8]) {
+    const uint32_t b0 = p[0], b1 = p[1];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        s[i] = sign_pair_mul(b0, mul[i]);
+        s[4 + i] = sign_pair_mul(b1, mul[i]);
+    }
 }
 
 template <int NTB>
@@ -111,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R::kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kConsumerWarps);
             mbar_init(&empty[s], kConsumerWarps);
         }
         *abort_flag = 0;
@@ -150,55 +164,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) accs[i][j] = 0.0f;
 
-    if (warp == kConsumerWarps) {
-        // ---- TMA producer ----
-        if (lane == 0) {
+    // ---- TMA issue, spread over the warps ----
+    // A step's boxes are W(k), W(k+64), x(k), x(k+64) and one bits box per
+    // variant; lane 0 of warp w issues boxes w and w + 16 and arrives on the
+    // slot's full barrier (16 arrivals) with their byte count.  Step j goes to
+    // slot j % kStages once all warps released that slot's previous step.  A
+    // warp blocks only for the step it is about to consume; otherwise it
+    // refills between its own steps without waiting.
+    const int n_boxes = 4 + a.nv;
+    auto box_bytes = [&](int bx) -> uint32_t { return bx < 2 ? kBoxBytes : bx < 4 ? R::kXBox : kBitsBox; };
+    const uint32_t my_tx = (warp < n_boxes ? box_bytes(warp) : 0u) + (warp + 16 < n_boxes ? box_bytes(warp + 16) : 0u);
+    int issued = 0;
+    auto issue_box = [&](int bx, int kc, uint8_t *st, uint64_t *bar) {
+        if (bx < 2)
+            tma_load_2d(st + bx * kBoxBytes, &maps.w, bar, kc + 64 * bx, row0);
+        else if (bx < 4)
+            tma_load_2d(st + 2 * kBoxBytes + (bx - 2) * R::kXBox, &maps.x, bar, kc + 64 * (bx - 2), 0);
+        else
+            tma_load_2d(st + 2 * kBoxBytes + 2 * R::kXBox + (bx - 4) * kBitsBox, &maps.b[bx - 4], bar, kc / 8, row0);
+    };
+    auto issue = [&](int j) {  // lane 0 only
+        const int s = j % R::kStages;
+        const int kc = static_cast<int>(k_lo) + j * kStepK;
+        uint8_t *st = smem + s * R::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], my_tx);
+        if (warp < n_boxes) issue_box(warp, kc, st, &full[s]);
+        if (warp + 16 < n_boxes) issue_box(warp + 16, kc, st, &full[s]);
+    };
+    if (lane == 0) {
+        if (warp == 0) {
             tma_prefetch_desc(&maps.w);
             tma_prefetch_desc(&maps.x);
-            const uint32_t tx = 2 * kBoxBytes + 2 * R::kXBox + a.nv * kBitsBox;
-            int issued = 0;
-            for (int i = 0; i < n_steps; ++i) {
-                const int s = i % R::kStages;
-                if (!mbar_wait(&empty[s], ((i / R::kStages) & 1) ^ 1, a.wait_ns, abort_flag)) {
-                    *abort_flag = 1;
-                    flag_status(a.status, kDevTimeout);
-                    break;
-                }
-                const int kc = static_cast<int>(k_lo) + i * kStepK;
-                uint8_t *st = smem + s * R::kStageBytes;
-                mbar_arrive_expect_tx(&full[s], tx);
-                tma_load_2d(st, &maps.w, &full[s], kc, row0);
-                tma_load_2d(st + kBoxBytes, &maps.w, &full[s], kc + 64, row0);
-                tma_load_2d(st + 2 * kBoxBytes, &maps.x, &full[s], kc, 0);
-                tma_load_2d(st + 2 * kBoxBytes + R::kXBox, &maps.x, &full[s], kc + 64, 0);
-                for (int v = 0; v < a.nv; ++v)
-                    tma_load_2d(st + 2 * kBoxBytes + 2 * R::kXBox + v * kBitsBox, &maps.b[v], &full[s], kc / 8, row0);
-                issued = i + 1;
-            }
-            if (*abort_flag) {  // drain this CTA's copies still in flight
-                for (int i = (issued > R::kStages ? issued - R::kStages : 0); i < issued; ++i)
-                    mbar_wait(&full[i % R::kStages], (i / R::kStages) & 1, kDrainLimitNs, nullptr);
-            }
         }
-    } else {
+        if (warp >= 4 && warp < n_boxes) tma_prefetch_desc(&maps.b[warp - 4]);
+        for (; issued < n_steps && issued < R::kStages; ++issued) issue(issued);
+    }
+    {
     // Constants of this warp's sign tiles q = 4i + tq (the same in every K step).
     const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ g) << 4);      // rows with (row & 7) == g
     const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ g) << 4);
     const int n_mine = n_st > tq ? (n_st - tq + 3) / 4 : 0;
     const int n_pairs = (n_mine + 1) / 2;
-    int x_off[NS], b_off[NS];  // x_off < 0: this lane's token row is past the tile
+    // A token row past its tile only feeds MMA column g, which the epilogue
+    // drops, so it reads some in-box row instead of being zeroed.
+    int x_off[NS], b_off[NS];
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
         const int q = 4 * i + tq;
-        const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
-        const int xr = start + g;
-        x_off[i] = g < cnt ? xr * 128 + (((2 * t) ^ (xr & 7)) << 4) : -1;
+        const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1];
+        const int xr = min(start + g, MP - 1);
+        x_off[i] = xr * 128 + (((2 * t) ^ (xr & 7)) << 4);
         b_off[i] = v * kBitsBox + r0 * 16 + 2 * t;
     }
 
     bool ok = true;
     for (int i = 0; i < n_steps; ++i) {
         const int s = i % R::kStages;
+        if (lane == 0) {
+            while (issued <= i) {  // this warp's part of the step is not in flight yet: wait for its slot
+                if (!mbar_wait(&empty[issued % R::kStages], ((issued / R::kStages) & 1) ^ 1, a.wait_ns,
+                               abort_flag)) {
+                    *abort_flag = 1;
+                    flag_status(a.status, kDevTimeout);
+                    break;
+                }
+                issue(issued);
+                ++issued;
+            }
+        }
         const bool got = mbar_wait(&full[s], (i / R::kStages) & 1, a.wait_ns, abort_flag);
         if (!__all_sync(0xFFFFFFFFu, got)) {
             if (lane == 0) {
@@ -240,13 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int i2 = 2 * ip + e < NS ? 2 * ip + e : NS - 1;
-                        signs8(*reinterpret_cast<const uint16_t *>(bits + b_off[i2]), sa[e]);
-                        signs8(*reinterpret_cast<const uint16_t *>(bits + b_off[i2] + 128), sb[e]);  // row r0 + 8
-                        uint4 p0 = make_uint4(0, 0, 0, 0), p1 = make_uint4(0, 0, 0, 0);
-                        if (x_off[i2] >= 0) {
-                            p0 = lds128(xbox + x_off[i2]);
-                            p1 = lds128(xbox + (x_off[i2] ^ 16));  // chunk 2t+1: flip the chunk's low bit
-                        }
+                        signs8(bits + b_off[i2], a.sign_mul, sa[e]);
+                        signs8(bits + b_off[i2] + 128, a.sign_mul, sb[e]);  // row r0 + 8
+                        const uint4 p0 = lds128(xbox + x_off[i2]);
+                        const uint4 p1 = lds128(xbox + (x_off[i2] ^ 16));  // chunk 2t+1: flip the chunk's low bit
                         xv[e][0] = p0.x, xv[e][1] = p0.y, xv[e][2] = p0.z, xv[e][3] = p0.w;
                         xv[e][4] = p1.x, xv[e][5] = p1.y, xv[e][6] = p1.z, xv[e][7] = p1.w;
                     }
@@ -262,6 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0) {  // refill every slot already released, without waiting
+            while (issued < n_steps &&
+                   mbar_test_wait(&empty[issued % R::kStages], ((issued / R::kStages) & 1) ^ 1)) {
+                issue(issued);
+                ++issued;
+            }
+        }
+    }
+    if (lane == 0 && *abort_flag) {  // drain this warp's copies still in flight
+        for (int i = (issued > R::kStages ? issued - R::kStages : 0); i < issued; ++i)
+            mbar_wait(&full[i % R::kStages], (i / R::kStages) & 1, kDrainLimitNs, nullptr);
     }
     (void)ok;
 
@@ -274,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p[0] = accb[ib][0], p[kRows] = accb[ib][1], p[8] = accb[ib][2], p[kRows + 8] = accb[ib][3];
         }
     }
-    asm volatile("bar.sync 1, 512;" ::: "memory");  // consumer warps only
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < NS; ++i) {  // alpha is constant along k: applied once to the full sign sums
         const int q = 4 * i + tq;
@@ -293,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    }  // consumers
+    }
     cluster.sync();
 
     // ---- rank c sums rows [c*share, (c+1)*share) over the cluster; scatter to original tokens ----
@@ -383,6 +424,7 @@ cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w
     a.n_in = n_in;
     a.status = ctx.status;
     a.wait_ns = ctx.wait_ns;
+    for (int i = 0; i < 4; ++i) a.sign_mul[i] = (1u << (15 - 2 * i)) + (1u << (30 - 2 * i));
     // K split over a cluster when the 64-row blocks leave SMs idle (one CTA per SM here).
     const int64_t row_blocks = (n_out + kRows - 1) / kRows;
     const int64_t steps = n_in / kStepK;
