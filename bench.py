@@ -142,22 +142,31 @@ def max_over_ranks(ws, value: float) -> float:
 class Phase:
     """A list of C-ABI calls replayed as one CUDA graph; algorithmic work per replay."""
 
-    def __init__(self, name, calls, bytes_=0.0, flops=0.0, launches=0, bound="hbm"):
+    def __init__(self, name, calls, bytes_=0.0, flops=0.0, launches=0, bound="hbm", weight_prefetch=False):
         self.name, self.calls, self.bytes, self.flops, self.launches, self.bound = \
             name, calls, bytes_, flops, launches, bound
+        self.weight_prefetch = weight_prefetch
         self.graph = None
 
     def run(self):
         for c in self.calls:
             c()
 
-    def capture(self, stream):
-        self.run()                     # eager warm-up: sets kernel attributes, caches device info
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            self.run()
-        self.graph = g
+    def capture(self, stream, bd=None):
+        """Graph of the calls.  With `weight_prefetch`, the launches are recorded with
+        bd_set_weight_prefetch(1): inside the graph every fused linear follows another
+        fused linear, which never writes weights, so the knob's condition holds."""
+        prev = bd.bd_set_weight_prefetch(1 if self.weight_prefetch else 0) if bd is not None else None
+        try:
+            self.run()                     # eager warm-up: sets kernel attributes, caches device info
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                self.run()
+            self.graph = g
+        finally:
+            if bd is not None:
+                bd.bd_set_weight_prefetch(prev)
 
     def replay(self):
         self.graph.replay()
@@ -176,6 +185,13 @@ def compress_phase(bd, mats, mode, dev):
         nbytes += 4.0 * n_out * n_in + n_out * n_in / 8 + 4.0 * (n_out if mode == 1 else 1)
         outs.append((bits, alpha))
     return Phase("compress", calls, bytes_=nbytes, launches=2 * len(mats)), outs
+
+
+# Fused linears of the device-resident decode/prefill phases are captured with
+# bd_set_weight_prefetch(1) (static weights, as when serving); --weight-prefetch 0
+# turns it off.  The end-to-end leg always runs with the library default (off),
+# since there a linear follows the compression that writes its bits.
+WEIGHT_PREFETCH = True
 
 
 def decode_bytes(m, n_out, n_in, mode):
@@ -236,7 +252,8 @@ class LayerWorkload(Workload):
                 nbytes += decode_bytes(m, n_out, n_in, mode)
                 flops += 2.0 * m * n_out * n_in
         bound = "hbm" if unit == "GB/s" else "tensor"
-        self.lin = Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=len(calls), bound=bound)
+        self.lin = Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=len(calls), bound=bound,
+                         weight_prefetch=WEIGHT_PREFETCH)
         self.phases = [self.comp, self.lin]
         self.dominant = self.lin
         self.h2d_tensors = [wf for (_, wf) in self.mats] + list(self.xs.values())
@@ -244,6 +261,7 @@ class LayerWorkload(Workload):
         self.config = {"workload": name, "matrices": sorted({f"{a}x{b}" for _, a, b in shapes}),
                        "matrix_count": len(shapes), "tokens": list(ms),
                        "alpha": "per-row" if mode == 1 else "scalar", "dtype_in": "bf16 weights/activations",
+                       "weight_prefetch": WEIGHT_PREFETCH,
                        "l2": "inputs larger than L2 (consecutive uses of a matrix separated by >250 MB of traffic)"}
 
     def oracle_sample(self, oracle, frac_rows: float):
@@ -381,7 +399,7 @@ def run_ours(args, ws, rank, local):
     wl = WORKLOADS[args.workload](bd, dev)
     stream = torch.cuda.Stream(device=dev)
     for p in wl.phases:
-        p.capture(stream)
+        p.capture(stream, bd)
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -620,6 +638,9 @@ def run_kernel_case(args):
         x = synth.activations(m, n_in, 7, dev)
         y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
 
+        torch.cuda.synchronize()  # the compressions above are complete before any linear is queued
+        bd.bd_set_weight_prefetch(1 if WEIGHT_PREFETCH else 0)  # the rotated copies are never written here
+
         def call(i):
             bd.bd_linear(x, mats[i][0], packed[i][0], packed[i][1], 0, y)
         work = decode_bytes(m, n_out, n_in, 0)
@@ -663,6 +684,7 @@ def run_kernel_case(args):
     assert bd.bd_get_device_status() == bd.BD_OK
     print(json.dumps({"kernel_case": args.kernel_case, "copies": copies, "launches_timed": reps,
                       "us_per_launch": med * 1e6, "GB/s": work / med / 1e9, "TFLOP/s": flops / med / 1e12,
+                      "weight_prefetch": WEIGHT_PREFETCH,
                       "env": {k: v for k, v in os.environ.items() if k.startswith("BD_")}}), flush=True)
 
 
@@ -675,9 +697,13 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama7b_layer_decode")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--weight-prefetch", type=int, choices=[0, 1], default=1,
+                    help="capture the device-resident fused linears with bd_set_weight_prefetch(1)")
     ap.add_argument("--kernel-case", default=None,
                     help="linear:N_OUTxN_IN:M[:path] or compress:N_OUTxN_IN[:mode] (one kernel, eager)")
     args = ap.parse_args()
+    global WEIGHT_PREFETCH
+    WEIGHT_PREFETCH = bool(args.weight_prefetch)
     if args.kernel_case:
         run_kernel_case(args)
         return

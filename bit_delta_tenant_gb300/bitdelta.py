@@ -59,6 +59,8 @@ def load_library(path: str | None = None):
         lib.bd_set_wait_limit_ns.restype = I64
         lib.bd_set_linear_path.argtypes = [I32]
         lib.bd_set_linear_path.restype = I32
+        lib.bd_set_weight_prefetch.argtypes = [I32]
+        lib.bd_set_weight_prefetch.restype = I32
         lib.bd_get_device_status.argtypes = [V]
         lib.bd_get_device_status.restype = I32
         lib.bd_compress_workspace_size.argtypes = [I64, I64, I32]
@@ -109,6 +111,10 @@ def bd_set_wait_limit_ns(limit_ns: int) -> int:
 
 def bd_set_linear_path(path: int) -> int:
     return int(load_library().bd_set_linear_path(int(path)))
+
+
+def bd_set_weight_prefetch(enable: int) -> int:
+    return int(load_library().bd_set_weight_prefetch(int(enable)))
 
 
 def bd_get_device_status(stream=None) -> int:

@@ -24,6 +24,7 @@ unsigned *g_status_ptr[kMaxDevices] = {nullptr};
 int g_num_sms[kMaxDevices] = {0};
 std::atomic<int64_t> g_wait_ns{-1};
 std::atomic<int32_t> g_linear_path{0};
+std::atomic<int32_t> g_weight_prefetch{0};
 
 int64_t wait_limit_ns() {
     int64_t v = g_wait_ns.load();
@@ -58,6 +59,7 @@ int32_t make_ctx(bd::DevCtx *ctx) {
         ctx->num_sms = g_num_sms[dev];
     }
     ctx->device = dev;
+    ctx->weight_prefetch = g_weight_prefetch.load() != 0;
     ctx->wait_ns = static_cast<uint64_t>(wait_limit_ns());
     return BD_OK;
 }
@@ -141,6 +143,10 @@ BD_API int32_t bd_set_linear_path(int32_t path) {
     const int32_t prev = g_linear_path.load();
     if (path >= 0 && path <= 3) g_linear_path.store(path);
     return prev;
+}
+
+BD_API int32_t bd_set_weight_prefetch(int32_t enable) {
+    return g_weight_prefetch.exchange(enable != 0 ? 1 : 0);
 }
 
 BD_API int32_t bd_get_device_status(void *stream) {

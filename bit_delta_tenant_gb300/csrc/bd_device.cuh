@@ -151,6 +151,9 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // Programmatic dependent launch: let the next kernel on the stream start its
 // prologue, then wait until every kernel this one depends on has completed
 // and its writes are visible.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void pdl_trigger_and_wait() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");

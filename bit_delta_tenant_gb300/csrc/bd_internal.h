@@ -21,6 +21,7 @@ struct DevCtx {
     uint64_t wait_ns;     // limit of every bounded wait
     int num_sms;          // SM count of the current device
     int device;           // current device ordinal
+    bool weight_prefetch; // weights may be read before the preceding kernel on the stream completes
 };
 
 // Device context of the current device (status word address, SM count, the

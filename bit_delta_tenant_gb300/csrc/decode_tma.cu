@@ -24,8 +24,10 @@
 // CTAs splits K; partials are added across the two halves in shared memory and
 // across the cluster through distributed shared memory, in a fixed order.
 // Launches allow programmatic dependent launch: the next kernel on the stream
-// may start its prologue while this one drains (every global read here comes
-// after griddepcontrol.wait, so data written by the previous kernel is seen).
+// may start its prologue while this one drains.  Every global read comes after
+// griddepcontrol.wait, so data written by the previous kernel is seen -- except,
+// when the caller enabled weight prefetch, the first stages' W_base and bits
+// boxes, which are issued before the wait.
 #include <cooperative_groups.h>
 
 #include <cstdlib>
@@ -63,6 +65,7 @@ struct TmaDecodeArgs {
     int64_t ks;
     int32_t mode;
     int32_t cluster;
+    int32_t prefetch_weights;  // issue the first stages' W and bits boxes before griddepcontrol.wait
     unsigned *status;
     uint64_t wait_ns;
 };
@@ -110,7 +113,23 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
         mbar_fence_init();
     }
     __syncthreads();
-    pdl_trigger_and_wait();
+    pdl_trigger();
+    const int n_pre = a.prefetch_weights ? min(n_steps, kStages) : 0;
+    if (warp == kConsumerWarps && lane == 0 && n_pre > 0) {
+        // Weights are not written by the preceding kernel (the caller's
+        // promise): start streaming them before that kernel completes.
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_b);
+        for (int i = 0; i < n_pre; ++i) {
+            const int kc = static_cast<int>(k_lo) + i * kStepK;
+            uint8_t *st = smem + i * kStageBytes;
+            mbar_arrive_expect_tx(&full[i], kStageBytes);
+            tma_load_2d(st, &tm_w, &full[i], kc, row0);
+            tma_load_2d(st + kBoxBytes, &tm_w, &full[i], kc + 64, row0);
+            tma_load_2d(st + 2 * kBoxBytes, &tm_b, &full[i], kc / 8, row0);
+        }
+    }
+    pdl_wait();
 
     float accb[NT][4], accs[NT][4];
 #pragma unroll
@@ -129,8 +148,14 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
             tma_prefetch_desc(&tm_w);
             tma_prefetch_desc(&tm_b);
             tma_prefetch_desc(&tm_x);
-            int issued = 0;
-            for (int i = 0; i < n_steps; ++i) {
+            for (int i = 0; i < n_pre; ++i) {  // the activations of the prefetched stages
+                const int kc = static_cast<int>(k_lo) + i * kStepK;
+                uint8_t *st = smem + i * kStageBytes;
+                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes, &tm_x, &full[i], kc, 0);
+                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes + kXBox, &tm_x, &full[i], kc + 64, 0);
+            }
+            int issued = n_pre;
+            for (int i = n_pre; i < n_steps; ++i) {
                 const int s = i % kStages;
                 const uint32_t ph = (i / kStages) & 1;
                 if (!mbar_wait(&empty[s], ph ^ 1, a.wait_ns, abort_flag)) {
@@ -185,17 +210,23 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
             const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
             const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
             const uint8_t *xrow = st + 2 * kBoxBytes + kBitsBytes + kh * kXBox + g * 128;
+            uint32_t xv[NT][8];
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt) {
                 const uint4 p0 = lds128(xrow + tt * 1024 + sw0);
                 const uint4 p1 = lds128(xrow + tt * 1024 + sw1);
-                const uint32_t xv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                xv[tt][0] = p0.x, xv[tt][1] = p0.y, xv[tt][2] = p0.z, xv[tt][3] = p0.w;
+                xv[tt][4] = p1.x, xv[tt][5] = p1.y, xv[tt][6] = p1.z, xv[tt][7] = p1.w;
+            }
+            // k-slice outer, tiles inner: consecutive MMAs never share an accumulator
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    mma_bf16_16816(accb[tt], wa[2 * j], wb[2 * j], wa[2 * j + 1], wb[2 * j + 1], xv[2 * j],
-                                   xv[2 * j + 1]);
-                    mma_bf16_16816(accs[tt], sa[2 * j], sb[2 * j], sa[2 * j + 1], sb[2 * j + 1], xv[2 * j],
-                                   xv[2 * j + 1]);
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int tt = 0; tt < NT; ++tt) {
+                    mma_bf16_16816(accb[tt], wa[2 * j], wb[2 * j], wa[2 * j + 1], wb[2 * j + 1], xv[tt][2 * j],
+                                   xv[tt][2 * j + 1]);
+                    mma_bf16_16816(accs[tt], sa[2 * j], sb[2 * j], sa[2 * j + 1], sb[2 * j + 1], xv[tt][2 * j],
+                                   xv[tt][2 * j + 1]);
                 }
             }
             __syncwarp();
@@ -356,6 +387,7 @@ cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, cons
     a.ks = p.ks;
     a.mode = alpha_mode;
     a.cluster = p.cluster;
+    a.prefetch_weights = ctx.weight_prefetch ? 1 : 0;
     a.status = ctx.status;
     a.wait_ns = ctx.wait_ns;
     switch (p.nt) {

@@ -213,6 +213,17 @@ int64_t bd_set_wait_limit_ns(int64_t limit_ns);
  * are ignored.  Returns the previous value. */
 int32_t bd_set_linear_path(int32_t path);
 
+/* Serving knob: when `enable` is non-zero, later bd_linear calls on the
+ * streaming path may start reading w_base and bits while the kernel launched
+ * just before them on the same stream is still finishing (programmatic
+ * dependent launch); x is read, and y written, only after that kernel has
+ * completed.  This overlaps the weight stream of back-to-back linears, as in
+ * a decode step over static weights.  Enable it only when no kernel that
+ * directly precedes a bd_linear on its stream writes that call's w_base or
+ * bits (for instance, not right after the bd_compress that produces the
+ * bits).  Default 0.  Returns the previous setting. */
+int32_t bd_set_weight_prefetch(int32_t enable);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t bd_version(void);
 

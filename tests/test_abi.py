@@ -131,3 +131,6 @@ def test_knobs_round_trip(lib):
     assert bd.bd_set_linear_path(p) == 2
     assert bd.bd_set_linear_path(9) == p          # out-of-range values are ignored
     assert bd.bd_set_linear_path(p) == p
+    w = bd.bd_set_weight_prefetch(1)
+    assert bd.bd_set_weight_prefetch(7) == 1          # any non-zero value enables
+    assert bd.bd_set_weight_prefetch(w) == 1

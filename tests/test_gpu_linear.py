@@ -179,3 +179,51 @@ def test_wait_limit_zero_reports_timeout_and_context_survives():
     assert bd.bd_get_device_status() == bd.BD_OK
     y_ref, mag = case.reference()
     assert_y_close(y_host(y), y_ref, mag, "after timeout")
+
+
+def with_weight_prefetch(enable: int):
+    class _Ctx:
+        def __enter__(self):
+            self.prev = bd.bd_set_weight_prefetch(enable)
+
+        def __exit__(self, *exc):
+            bd.bd_set_weight_prefetch(self.prev)
+    return _Ctx()
+
+
+@pytest.mark.parametrize("m", [1, 16, 64])
+def test_weight_prefetch_chain_in_a_graph(m):
+    """Back-to-back streaming linears captured in a CUDA graph with weight
+    prefetch on: each kernel may read its weights while the previous one
+    drains, but its activations only after that kernel completes.  The chain
+    feeds y of the first linear into the second (a read-after-write through x),
+    so a stale read would show up in the second output."""
+    a = LinearCase(384, 1024, m, seed=21)
+    b = LinearCase(640, 384, 0, seed=22)
+    c = LinearCase(512, 2048, m, seed=23)
+    s = torch.cuda.Stream()
+
+    def chain(prefetch):
+        y1 = torch.full((m, 384), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y2 = torch.full((m, 640), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y3 = torch.full((m, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        with with_linear_path(STREAM), with_weight_prefetch(prefetch):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                bd.bd_linear(a.x, a.w_base, a.bits, a.alpha, 0, y1, s)
+                bd.bd_linear(y1, b.w_base, b.bits, b.alpha, 0, y2, s)
+                bd.bd_linear(c.x, c.w_base, c.bits, c.alpha, 0, y3, s)
+        g.replay()
+        torch.cuda.synchronize()
+        assert bd.bd_get_device_status() == bd.BD_OK
+        return y1, y2, y3
+
+    p1, p2, p3 = chain(1)
+    q1, q2, q3 = chain(0)
+    for y, case in ((p1, a), (p3, c)):
+        y_ref, mag = case.reference()
+        assert_y_close(y_host(y), y_ref, mag, f"prefetch m={m}")
+    # the same kernels in the same order: identical bits with and without prefetch
+    assert torch.equal(p1, q1) and torch.equal(p3, q3)
+    assert torch.equal(p2, q2), "the dependent linear read its activations before they were written"
