@@ -212,7 +212,7 @@ BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uin
     if (rc != BD_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int32_t path = g_linear_path.load();
-    const bool tma_ok = bd::decode_tma_supported(m, n_out, n_in, w_base, bits, ctx.num_sms);
+    const bool tma_ok = bd::decode_tma_supported(m, n_out, n_in, w_base, bits, ctx);
     const bool decode_ok = tma_ok || bd::decode_supported(m, n_out, n_in, ctx.num_sms);
     bool use_decode = decode_ok && m <= bd::kDecodeMaxM;
     if (path == 1) {

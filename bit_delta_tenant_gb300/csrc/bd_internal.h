@@ -56,7 +56,7 @@ cudaError_t launch_decode(const void *x, int64_t m, const void *w_base, const ui
 // TMA-fed variant of the streaming kernel (n_in % 128 == 0, 16-byte aligned
 // W_base and bits); preferred whenever it applies.
 bool decode_tma_supported(int64_t m, int64_t n_out, int64_t n_in, const void *w_base, const uint8_t *bits,
-                          int num_sms);
+                          const DevCtx &ctx);
 cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                               int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                               cudaStream_t stream);

@@ -3,8 +3,8 @@
 // y = x.W_base^T + alpha * (x.S^T) on mma.m16n8k16, signs built in registers),
 // but W_base, the packed bits and the activations arrive through a multi-stage
 // ring of shared-memory tiles filled by one producer warp with cp.async.bulk.tensor,
-// so each SM keeps tens of KB of HBM reads in flight for a handful of
-// instructions, and two CTAs fit on an SM.
+// so each SM keeps well over 100 KB of HBM reads in flight for a handful of
+// instructions.
 //
 // Method: "BitDelta : servir 14 modèles Zen depuis un seul cluster GPU"
 // (Hanzo blog), section "Architecture de service": one fused kernel reads
@@ -12,17 +12,20 @@
 // weight on chip, never writing W_eff to HBM (conceptual fused_bitdelta_linear
 // listing).
 //
-// CTA: 8 consumer warps + 1 producer warp; 64 W rows; a stage is a 128-column
-// K step: two 64x64 bf16 W boxes (128-byte swizzle), one 64x16-byte box of
-// packed bits and two (8*NT tokens x 64 columns) activation boxes (128-byte
-// swizzle; rows beyond m arrive as zeros).  Consumer warp w owns row group w%4 (16 rows, the M side of the
-// MMA) and 64-column half w/4 of every stage.  Lane (g, t) reads 16-byte
-// chunks 2t and 2t+1 of rows g and g+8 -- with the swizzle the eight lanes of a
-// shared-memory phase hit eight different bank groups -- so its 16 columns are
-// 16t..16t+15 of the half, and the k-slots of the four MMAs per half map to
-// those columns in order, identically for the activations.  A cluster of C
-// CTAs splits K; partials are added across the two halves in shared memory and
-// across the cluster through distributed shared memory, in a fixed order.
+// CTA (one per SM): R row groups of 16 W rows (R = 1..8, chosen per shape so
+// that the busiest SM streams as little as possible), 2R consumer warps + 1
+// producer warp.  A stage is a 128-column K step: two (16R x 64) bf16 W boxes
+// (128-byte swizzle), one 16R x 16-byte box of packed bits and two (8*NT
+// tokens x 64 columns) activation boxes (128-byte swizzle; rows beyond m
+// arrive as zeros).  Consumer warp w owns row group w % R (16 rows, the M side
+// of the MMA) and 64-column half w / R of every stage.  Lane (g, t) reads
+// 16-byte chunks 2t and 2t+1 of rows g and g+8 -- with the swizzle the eight
+// lanes of a shared-memory phase hit eight different bank groups -- so its 16
+// columns are 16t..16t+15 of the half, and the k-slots of the four MMAs per
+// half map to those columns in order, identically for the activations.  A
+// cluster of C CTAs splits K; partials are added across the two halves in
+// shared memory and across the cluster through distributed shared memory, in
+// a fixed order.
 // Launches allow programmatic dependent launch: the next kernel on the stream
 // may start its prologue while this one drains.  Every global read comes after
 // griddepcontrol.wait, so data written by the previous kernel is seen -- except,
@@ -30,6 +33,7 @@
 // boxes, which are issued before the wait.
 #include <cooperative_groups.h>
 
+#include <cstdio>
 #include <cstdlib>
 
 #include "bd_device.cuh"
@@ -40,23 +44,33 @@ namespace cg = cooperative_groups;
 namespace bd {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 288
-constexpr int kRows = 64;                            // W rows per CTA
-constexpr int kStepK = 128;                          // K columns per stage
-constexpr uint32_t kBoxBytes = 64 * 64 * 2;          // one 64-row x 64-column bf16 box
-constexpr uint32_t kBitsBytes = kRows * 16;          // 64 rows x 16 packed bytes (128 columns)
+constexpr int kStepK = 128;                 // K columns per stage
+constexpr int kMaxSmem = 227 * 1024;        // opt-in dynamic shared memory per CTA on sm_103
+constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory of one SM (1 KB of it reserved per CTA)
 
-// Per token-tile count NT (8 tokens each): ring depth, and the stage layout
-// [W box k0..63][W box k64..127][bits][x box k0..63][x box k64..127]; every box
-// starts on a 1024-byte boundary (the 128-byte swizzle pattern repeats there).
-template <int NT> struct Ring {
-    static constexpr int kStages = NT == 1 ? 5 : NT == 2 ? 4 : NT == 4 ? 7 : 6;
-    static constexpr uint32_t kXBox = 8 * NT * 128;  // MP tokens x 64 columns
-    static constexpr uint32_t kStageBytes = 2 * kBoxBytes + kBitsBytes + 2 * kXBox;
-    static constexpr uint32_t kRedBytes = 8 * NT * kRows * 4;
-    static constexpr size_t kSmem = 1024 + kStages * kStageBytes + kRedBytes + 2 * kStages * 8 + 16;
+// Stage layout for R row groups (rows = 16R) and NT token tiles (MP = 8NT):
+// [W box k0..63: rows x 128 B][W box k64..127][bits: rows x 16 B, padded to
+// 1 KB][x box k0..63: MP x 128 B][x box k64..127]; every box starts on a
+// 1024-byte boundary (the 128-byte swizzle pattern repeats there).
+struct StageLayout {
+    uint32_t w_box, bits_off, bits_bytes, x_off, x_box, stage, tx;
 };
+__host__ __device__ constexpr StageLayout stage_layout(int rg, int nt) {
+    StageLayout L{};
+    const uint32_t rows = 16u * rg;
+    L.w_box = rows * 128u;
+    L.bits_off = 2u * L.w_box;
+    L.bits_bytes = rows * 16u;
+    L.x_off = L.bits_off + (L.bits_bytes + 1023u) / 1024u * 1024u;
+    L.x_box = 1024u * nt;
+    L.stage = L.x_off + 2u * L.x_box;
+    L.tx = 2u * L.w_box + L.bits_bytes + 2u * L.x_box;  // bytes the copies deliver
+    return L;
+}
+__host__ __device__ constexpr uint32_t red_bytes(int rg, int nt) { return 8u * nt * 16u * rg * 4u; }
+inline size_t smem_bytes(int rg, int nt, int stages) {
+    return 1024 + static_cast<size_t>(stages) * stage_layout(rg, nt).stage + red_bytes(rg, nt) + 2 * stages * 8 + 16;
+}
 
 struct TmaDecodeArgs {
     const float *alpha;
@@ -65,12 +79,12 @@ struct TmaDecodeArgs {
     int64_t ks;
     int32_t mode;
     int32_t cluster;
+    int32_t rg;                // row groups of 16 rows per CTA
+    int32_t stages;            // ring depth
     int32_t prefetch_weights;  // issue the first stages' W and bits boxes before griddepcontrol.wait
     unsigned *status;
     uint64_t wait_ns;
 };
-
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
@@ -79,35 +93,38 @@ __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *stat
     flag_status(status, kDevTimeout);
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
+template <int NT, int RG>
+__global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ TmaDecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int MP = 8 * NT;
-    constexpr int kStages = Ring<NT>::kStages;
-    constexpr uint32_t kStageBytes = Ring<NT>::kStageBytes;
-    constexpr uint32_t kXBox = Ring<NT>::kXBox;
+    constexpr int rg_n = RG;
+    constexpr int rows = 16 * RG;
+    constexpr int n_cons = 2 * RG;  // consumer warps: row group w % R, K half w / R
+    const int kStages = a.stages;
+    constexpr StageLayout L = stage_layout(RG, NT);
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *red = reinterpret_cast<float *>(smem + kStages * kStageBytes);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes + Ring<NT>::kRedBytes);
+    float *red = reinterpret_cast<float *>(smem + kStages * L.stage);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * L.stage + red_bytes(rg_n, NT));
     uint64_t *empty = full + kStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
     const int64_t row_block = blockIdx.x / a.cluster;
-    const int row0 = static_cast<int>(row_block * kRows);
+    const int row0 = static_cast<int>(row_block * rows);
     const int64_t k_lo = static_cast<int64_t>(rank) * a.ks;
     const int64_t k_hi = min(k_lo + a.ks, a.n_in);
     const int n_steps = k_hi > k_lo ? static_cast<int>((k_hi - k_lo + kStepK - 1) / kStepK) : 0;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const bool is_producer = warp == n_cons;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], n_cons);
         }
         *abort_flag = 0;
         mbar_fence_init();
@@ -115,18 +132,18 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
     __syncthreads();
     pdl_trigger();
     const int n_pre = a.prefetch_weights ? min(n_steps, kStages) : 0;
-    if (warp == kConsumerWarps && lane == 0 && n_pre > 0) {
+    if (is_producer && lane == 0 && n_pre > 0) {
         // Weights are not written by the preceding kernel (the caller's
         // promise): start streaming them before that kernel completes.
         tma_prefetch_desc(&tm_w);
         tma_prefetch_desc(&tm_b);
         for (int i = 0; i < n_pre; ++i) {
             const int kc = static_cast<int>(k_lo) + i * kStepK;
-            uint8_t *st = smem + i * kStageBytes;
-            mbar_arrive_expect_tx(&full[i], kStageBytes);
+            uint8_t *st = smem + i * L.stage;
+            mbar_arrive_expect_tx(&full[i], L.tx);
             tma_load_2d(st, &tm_w, &full[i], kc, row0);
-            tma_load_2d(st + kBoxBytes, &tm_w, &full[i], kc + 64, row0);
-            tma_load_2d(st + 2 * kBoxBytes, &tm_b, &full[i], kc / 8, row0);
+            tma_load_2d(st + L.w_box, &tm_w, &full[i], kc + 64, row0);
+            tma_load_2d(st + L.bits_off, &tm_b, &full[i], kc / 8, row0);
         }
     }
     pdl_wait();
@@ -138,11 +155,11 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
         for (int j = 0; j < 4; ++j) accb[i][j] = accs[i][j] = 0.0f;
 
     const int g = lane >> 2, t = lane & 3;
-    const int rg = warp & 3;       // row group
-    const int kh = warp >> 2;      // 64-column half of each stage
-    const int r0 = rg * 16 + g;    // tile rows r0, r0 + 8
+    const int rgi = warp % rg_n;   // row group
+    const int kh = warp / rg_n;    // 64-column half of each stage
+    const int r0 = rgi * 16 + g;   // tile rows r0, r0 + 8
 
-    if (warp == kConsumerWarps) {
+    if (is_producer) {
         // ---- producer ----
         if (lane == 0) {
             tma_prefetch_desc(&tm_w);
@@ -150,26 +167,26 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
             tma_prefetch_desc(&tm_x);
             for (int i = 0; i < n_pre; ++i) {  // the activations of the prefetched stages
                 const int kc = static_cast<int>(k_lo) + i * kStepK;
-                uint8_t *st = smem + i * kStageBytes;
-                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes, &tm_x, &full[i], kc, 0);
-                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes + kXBox, &tm_x, &full[i], kc + 64, 0);
+                uint8_t *st = smem + i * L.stage;
+                tma_load_2d(st + L.x_off, &tm_x, &full[i], kc, 0);
+                tma_load_2d(st + L.x_off + L.x_box, &tm_x, &full[i], kc + 64, 0);
             }
             int issued = n_pre;
-            for (int i = n_pre; i < n_steps; ++i) {
-                const int s = i % kStages;
-                const uint32_t ph = (i / kStages) & 1;
+            int s = n_pre % kStages;  // slot and phase advance incrementally (the ring depth is a launch value)
+            uint32_t ph = (n_pre / kStages) & 1;
+            for (int i = n_pre; i < n_steps; ++i, (++s == kStages ? (s = 0, ph ^= 1u) : 0u)) {
                 if (!mbar_wait(&empty[s], ph ^ 1, a.wait_ns, abort_flag)) {
                     give_up(abort_flag, a.status);
                     break;
                 }
                 const int kc = static_cast<int>(k_lo) + i * kStepK;
-                uint8_t *st = smem + s * kStageBytes;
-                mbar_arrive_expect_tx(&full[s], kStageBytes);
+                uint8_t *st = smem + s * L.stage;
+                mbar_arrive_expect_tx(&full[s], L.tx);
                 tma_load_2d(st, &tm_w, &full[s], kc, row0);
-                tma_load_2d(st + kBoxBytes, &tm_w, &full[s], kc + 64, row0);
-                tma_load_2d(st + 2 * kBoxBytes, &tm_b, &full[s], kc / 8, row0);
-                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes, &tm_x, &full[s], kc, 0);
-                tma_load_2d(st + 2 * kBoxBytes + kBitsBytes + kXBox, &tm_x, &full[s], kc + 64, 0);
+                tma_load_2d(st + L.w_box, &tm_w, &full[s], kc + 64, row0);
+                tma_load_2d(st + L.bits_off, &tm_b, &full[s], kc / 8, row0);
+                tma_load_2d(st + L.x_off, &tm_x, &full[s], kc, 0);
+                tma_load_2d(st + L.x_off + L.x_box, &tm_x, &full[s], kc + 64, 0);
                 issued = i + 1;
             }
             if (*abort_flag) {
@@ -182,21 +199,21 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
         // Token rows of the x boxes use the same swizzle term as W rows: (8*tt + g) & 7 == r0 & 7 == g.
         const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ (r0 & 7)) << 4);
         const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ (r0 & 7)) << 4);  // rows r0, r0+8 share r&7
-        for (int i = 0; i < n_steps; ++i) {
-            const int s = i % kStages;
-            const uint32_t ph = (i / kStages) & 1;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < n_steps; ++i, (++s == kStages ? (s = 0, ph ^= 1u) : 0u)) {
             const bool got = mbar_wait(&full[s], ph, a.wait_ns, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 if (lane == 0) give_up(abort_flag, a.status);
                 break;
             }
-            const uint8_t *st = smem + s * kStageBytes;
-            const uint8_t *box = st + kh * kBoxBytes;
+            const uint8_t *st = smem + s * L.stage;
+            const uint8_t *box = st + kh * L.w_box;
             const uint4 wa0 = lds128(box + r0 * 128 + sw0);
             const uint4 wa1 = lds128(box + r0 * 128 + sw1);
             const uint4 wb0 = lds128(box + (r0 + 8) * 128 + sw0);
             const uint4 wb1 = lds128(box + (r0 + 8) * 128 + sw1);
-            const uint8_t *bt = st + 2 * kBoxBytes;
+            const uint8_t *bt = st + L.bits_off;
             const uint32_t ba = *reinterpret_cast<const uint16_t *>(bt + r0 * 16 + kh * 8 + 2 * t);
             const uint32_t bb = *reinterpret_cast<const uint16_t *>(bt + (r0 + 8) * 16 + kh * 8 + 2 * t);
             const uint32_t ba0 = ba & 0xFFu, ba1 = ba >> 8, bb0 = bb & 0xFFu, bb1 = bb >> 8;
@@ -209,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
                                     sign_pair_bf16<2>(bb1), sign_pair_bf16<3>(bb1)};
             const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
             const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
-            const uint8_t *xrow = st + 2 * kBoxBytes + kBitsBytes + kh * kXBox + g * 128;
+            const uint8_t *xrow = st + L.x_off + kh * L.x_box + g * 128;
             uint32_t xv[NT][8];
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt) {
@@ -251,36 +268,36 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt) {
                 const int c = 8 * tt + 2 * t;
-                red[c * kRows + r0] = part[tt][0];
-                red[(c + 1) * kRows + r0] = part[tt][1];
-                red[c * kRows + r0 + 8] = part[tt][2];
-                red[(c + 1) * kRows + r0 + 8] = part[tt][3];
+                red[c * rows + r0] = part[tt][0];
+                red[(c + 1) * rows + r0] = part[tt][1];
+                red[c * rows + r0 + 8] = part[tt][2];
+                red[(c + 1) * rows + r0 + 8] = part[tt][3];
             }
         }
-        consumer_sync();
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * n_cons) : "memory");  // consumer warps only
         if (kh == 0) {
 #pragma unroll
             for (int tt = 0; tt < NT; ++tt) {
                 const int c = 8 * tt + 2 * t;
-                red[c * kRows + r0] += part[tt][0];
-                red[(c + 1) * kRows + r0] += part[tt][1];
-                red[c * kRows + r0 + 8] += part[tt][2];
-                red[(c + 1) * kRows + r0 + 8] += part[tt][3];
+                red[c * rows + r0] += part[tt][0];
+                red[(c + 1) * rows + r0] += part[tt][1];
+                red[c * rows + r0 + 8] += part[tt][2];
+                red[(c + 1) * rows + r0 + 8] += part[tt][3];
             }
         }
     }
     cluster.sync();
 
     // ---- rank c sums rows [c*share, (c+1)*share) of the block over the cluster ----
-    const int share = (kRows + a.cluster - 1) / a.cluster;
+    const int share = (rows + a.cluster - 1) / a.cluster;
     const int m_here = static_cast<int>(a.m < MP ? a.m : MP);
-    for (int i = threadIdx.x; i < share * m_here; i += kThreads) {
+    for (int i = threadIdx.x; i < share * m_here; i += blockDim.x) {
         const int tok = i / share;
         const int lr = rank * share + (i - tok * share);
         const int64_t row = static_cast<int64_t>(row0) + lr;
-        if (lr < kRows && row < a.n_out) {
+        if (lr < rows && row < a.n_out) {
             float s = 0.0f;
-            for (int q = 0; q < a.cluster; ++q) s += cluster.map_shared_rank(red, q)[tok * kRows + lr];
+            for (int q = 0; q < a.cluster; ++q) s += cluster.map_shared_rank(red, q)[tok * rows + lr];
             __nv_bfloat16 h = __float2bfloat16_rn(s);
             a.y[static_cast<int64_t>(tok) * a.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
         }
@@ -289,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, NT <= 2 ? 2 : 1)
 }
 
 struct TmaPlan {
-    int nt, cluster;
+    int nt, cluster, rg, stages;
     int64_t ks, row_blocks;
 };
 
@@ -300,42 +317,104 @@ int env_int(const char *name, int dflt) {
     return v > 0 ? v : dflt;
 }
 
-bool make_tma_plan(int64_t m, int64_t n_out, int64_t n_in, int num_sms, TmaPlan &p) {
-    if (m < 1 || m > kDecodeMaxM) return false;
+template <int NT, int RG>
+cudaError_t ensure_smem_attr(int device) {
+    static bool attr_set[128] = {false};
+    if (device >= 0 && device < 128 && attr_set[device]) return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_tma_kernel<NT, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess && device >= 0 && device < 128) attr_set[device] = true;
+    return e;
+}
+
+// The (NT, R) pairs the plan can produce are instantiated: R = 4 everywhere,
+// 5..8 for m <= 16 (the balanced split of row counts just above 64 x SMs),
+// 7 for m <= 32.
+bool plan_instantiated(int nt, int rg) { return rg == 4 || (nt <= 2 && rg >= 5 && rg <= 8) || (nt == 4 && rg == 7); }
+
+// Deepest ring whose CTA fits in `budget` bytes of shared memory.
+int stages_within(int rg, int nt, size_t budget) {
+    int s = 8;
+    while (s > 0 && smem_bytes(rg, nt, s) > budget) --s;
+    return s;
+}
+
+// Launch plan: R (16-row groups per CTA), C (ranks splitting K in a
+// cluster) and the ring depth, from sweeps of this kernel on GB300 (rows x
+// K from 1024 x 4096 to 28672 x 8192, m = 1 .. 64):
+//  * m <= 16: 64-row CTAs (R = 4), two per SM (rings of 5 / 4 stages of
+//    19 / 21 KB), which lets the next launch's CTAs start prefetching on an
+//    SM while this launch's second CTA drains.  K is split over a cluster
+//    when the row blocks alone leave SMs idle: C = ceil(1.5 * SMs / blocks).
+//    When the 64-row blocks exceed the SM count by at most a quarter (11008
+//    rows -> 172 blocks), some SMs would stream two blocks while others
+//    stream one; there R = ceil(groups / SMs) row groups per block, split in
+//    two along K, puts two equal half-blocks on nearly every SM instead
+//    (measured 17.4 us against 21.9 us for 11008 x 4096).
+//  * 16 < m <= 32: the widest CTA the registers allow (R = 7, 14 consumer
+//    warps), one per SM, when its blocks times a K split fill at least 90% of
+//    the SMs in one wave -- the MMA work per byte has grown (8192 x 8192:
+//    35.6 us against 44.5 us with R = 4); otherwise as below.
+//  * 32 < m <= 64: R = 4, one CTA per SM.
+// BD_DECODE_ROW_GROUPS / BD_DECODE_CLUSTER / BD_DECODE_STAGES override the
+// three choices (sweeps).
+bool make_tma_plan(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx, TmaPlan &p) {
+    const int num_sms = ctx.num_sms;
+    if (m < 1 || m > kDecodeMaxM || n_out < 1 || n_in < 1 || num_sms < 1) return false;
     p.nt = m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8;
-    p.row_blocks = (n_out + kRows - 1) / kRows;
-    // Split K over a cluster only when the 64-row blocks alone leave SMs idle:
-    // each split adds a reduction, an activation re-read and cluster placement
-    // constraints.  Measured on GB300: one split when row blocks >= SMs; about
-    // 1.5 CTAs per SM otherwise (4096 rows -> 4 splits).
-    int c = 1;
-    if (p.row_blocks < num_sms)
-        c = static_cast<int>((3 * static_cast<int64_t>(num_sms) / 2 + p.row_blocks - 1) / p.row_blocks);
-    c = env_int("BD_DECODE_CLUSTER", c);
-    if (c < 1) c = 1;
-    if (c > 8) c = 8;
+    const int64_t groups = (n_out + 15) / 16;
     const int64_t steps = (n_in + kStepK - 1) / kStepK;
+    int rg = 4;
+    int c = 0;
+    int stages = p.nt == 1 ? 5 : p.nt == 2 ? 4 : 8;
+    const int64_t blocks7 = (groups + 6) / 7;
+    if (p.nt == 4 && blocks7 <= num_sms) {
+        const int64_t c7 = num_sms / blocks7 < 8 ? num_sms / blocks7 : 8;
+        if (10 * blocks7 * c7 >= 9 * static_cast<int64_t>(num_sms)) rg = 7, c = static_cast<int>(c7);
+    }
+    const int64_t blocks4 = (groups + 3) / 4;
+    if (p.nt <= 2 && blocks4 > num_sms && 4 * blocks4 <= 5 * static_cast<int64_t>(num_sms)) {
+        const int64_t r = (groups + num_sms - 1) / num_sms;
+        if (r <= 8) {
+            rg = static_cast<int>(r);
+            c = 2;
+            stages = stages_within(rg, p.nt, kSmemPerSm / 2 - 1024);
+        }
+    }
+    rg = env_int("BD_DECODE_ROW_GROUPS", rg);
+    if (!plan_instantiated(p.nt, rg)) rg = 4;
+    const int64_t blocks = (groups + rg - 1) / rg;
+    if (c == 0) c = blocks >= num_sms ? 1 : static_cast<int>((3 * static_cast<int64_t>(num_sms) / 2 + blocks - 1) / blocks);
+    c = env_int("BD_DECODE_CLUSTER", c);
+    if (c > 8) c = 8;
     if (c > steps) c = static_cast<int>(steps);
+    stages = env_int("BD_DECODE_STAGES", stages);
+    const int deepest = stages_within(rg, p.nt, kMaxSmem);
+    if (stages > deepest) stages = deepest;
+    if (stages < 3) return false;
     const int64_t per = (steps + c - 1) / c;
+    p.rg = rg;
+    p.stages = stages;
     p.ks = per * kStepK;
     p.cluster = static_cast<int>((steps + per - 1) / per);  // no empty ranks
+    p.row_blocks = blocks;
+    if (p.row_blocks * p.cluster > 0x7FFFFFFFLL) return false;
+    if (std::getenv("BD_DECODE_PLAN_VERBOSE"))  // debug: the plan of every launch
+        std::fprintf(stderr, "decode plan m<=%d %lldx%lld: R=%d C=%d stages=%d CTAs=%lld\n", 8 * p.nt,
+                     static_cast<long long>(n_out), static_cast<long long>(n_in), p.rg, p.cluster, p.stages,
+                     static_cast<long long>(p.row_blocks * p.cluster));
     return true;
 }
 
-template <int NT>
-cudaError_t launch_nt(const CUtensorMap &tw, const CUtensorMap &tb, const CUtensorMap &tx, const TmaDecodeArgs &a,
-                      const TmaPlan &p, const DevCtx &ctx, cudaStream_t stream) {
-    static bool attr_set[128] = {false};
-    if (ctx.device < 128 && !attr_set[ctx.device]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_tma_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(Ring<NT>::kSmem));
-        if (e != cudaSuccess) return e;
-        attr_set[ctx.device] = true;
-    }
+template <int NT, int RG>
+cudaError_t launch_plan(const CUtensorMap &tw, const CUtensorMap &tb, const CUtensorMap &tx, const TmaDecodeArgs &a,
+                        const TmaPlan &p, const DevCtx &ctx, cudaStream_t stream) {
+    cudaError_t e = ensure_smem_attr<NT, RG>(ctx.device);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.row_blocks * p.cluster), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Ring<NT>::kSmem;
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * (2 * RG + 1)), 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes(RG, NT, p.stages);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -346,31 +425,42 @@ cudaError_t launch_nt(const CUtensorMap &tw, const CUtensorMap &tb, const CUtens
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_tma_kernel<NT>, tw, tb, tx, a);
+    return cudaLaunchKernelEx(&cfg, decode_tma_kernel<NT, RG>, tw, tb, tx, a);
+}
+
+cudaError_t launch_any(const CUtensorMap &tw, const CUtensorMap &tb, const CUtensorMap &tx, const TmaDecodeArgs &a,
+                       const TmaPlan &p, const DevCtx &ctx, cudaStream_t stream) {
+#define BD_DECODE_CASE(NT_, RG_) \
+    if (p.nt == NT_ && p.rg == RG_) return launch_plan<NT_, RG_>(tw, tb, tx, a, p, ctx, stream);
+    BD_DECODE_CASE(1, 4) BD_DECODE_CASE(1, 5) BD_DECODE_CASE(1, 6) BD_DECODE_CASE(1, 7) BD_DECODE_CASE(1, 8)
+    BD_DECODE_CASE(2, 4) BD_DECODE_CASE(2, 5) BD_DECODE_CASE(2, 6) BD_DECODE_CASE(2, 7) BD_DECODE_CASE(2, 8)
+    BD_DECODE_CASE(4, 4) BD_DECODE_CASE(4, 7) BD_DECODE_CASE(8, 4)
+#undef BD_DECODE_CASE
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
 
 bool decode_tma_supported(int64_t m, int64_t n_out, int64_t n_in, const void *w_base, const uint8_t *bits,
-                          int num_sms) {
+                          const DevCtx &ctx) {
     if (n_in % kStepK != 0) return false;  // packed-bit rows must be 16-byte multiples for TMA
     if ((reinterpret_cast<uintptr_t>(w_base) & 15) || (reinterpret_cast<uintptr_t>(bits) & 15)) return false;
     if (n_in >= (int64_t(1) << 31) - kStepK) return false;
     TmaPlan p;
-    return make_tma_plan(m, n_out, n_in, num_sms, p);
+    return make_tma_plan(m, n_out, n_in, ctx, p);
 }
 
 cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                               int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                               cudaStream_t stream) {
     TmaPlan p;
-    if (!make_tma_plan(m, n_out, n_in, ctx.num_sms, p)) return cudaErrorNotSupported;
-    if (p.row_blocks * p.cluster > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (!make_tma_plan(m, n_out, n_in, ctx, p)) return cudaErrorNotSupported;
+    const uint32_t rows = static_cast<uint32_t>(16 * p.rg);
     CUtensorMap tw, tb;
-    if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, 64, kRows,
+    if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, 64, rows,
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bits, n_in / 8, n_out, n_in / 8, 16, kRows,
+    if (!encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bits, n_in / 8, n_out, n_in / 8, 16, rows,
                               CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const int mp = 8 * p.nt;
@@ -387,15 +477,12 @@ cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, cons
     a.ks = p.ks;
     a.mode = alpha_mode;
     a.cluster = p.cluster;
+    a.rg = p.rg;
+    a.stages = p.stages;
     a.prefetch_weights = ctx.weight_prefetch ? 1 : 0;
     a.status = ctx.status;
     a.wait_ns = ctx.wait_ns;
-    switch (p.nt) {
-        case 1: return launch_nt<1>(tw, tb, tx, a, p, ctx, stream);
-        case 2: return launch_nt<2>(tw, tb, tx, a, p, ctx, stream);
-        case 4: return launch_nt<4>(tw, tb, tx, a, p, ctx, stream);
-        default: return launch_nt<8>(tw, tb, tx, a, p, ctx, stream);
-    }
+    return launch_any(tw, tb, tx, a, p, ctx, stream);
 }
 
 }  // namespace bd
