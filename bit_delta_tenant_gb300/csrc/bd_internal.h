@@ -30,8 +30,8 @@ int32_t make_dev_ctx(DevCtx *ctx);
 
 // ---- compression -------------------------------------------------------------------
 constexpr int kCompressThreads = 256;
-constexpr int kCompressChunksPerThread = 8;                                        // 16-byte chunks
-constexpr int64_t kCompressChunksPerSeg = kCompressThreads * kCompressChunksPerThread;  // 2048 chunks
+constexpr int kCompressChunksPerThread = 4;                                        // 16-byte chunks
+constexpr int64_t kCompressChunksPerSeg = kCompressThreads * kCompressChunksPerThread;  // 1024 chunks
 
 // Geometry of the deterministic two-level reduction: `rows` independent sums
 // (1 for a scalar alpha, n_out per-row), each over `row_chunks` chunks of 8

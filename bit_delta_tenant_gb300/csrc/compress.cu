@@ -18,11 +18,12 @@
 // owns 16-byte chunks (8 bf16) of both inputs, so one chunk yields exactly one
 // output byte in registers with no cross-lane exchange, and lanes own
 // consecutive chunks, so the byte stores are 32-byte coalesced.  |Delta| is
-// summed pairwise in fp32 per thread (64 terms), widened to fp64, reduced
+// summed pairwise in fp32 per thread (32 terms), widened to fp64, reduced
 // through the warp with xor-shuffles and across warps in a fixed order: one
-// fp64 partial per 2048-chunk segment.  A second kernel adds each row's
+// fp64 partial per 1024-chunk segment.  A second kernel adds each row's
 // partials in a fixed order and rounds alpha to fp32 once, so alpha is bitwise
-// reproducible for a given shape on any device.
+// reproducible for a given shape on any device; a row that is a single
+// segment (per-row alpha, n_in <= 16384) gets its alpha from pass 1 directly.
 #include "bd_device.cuh"
 #include "bd_internal.h"
 
@@ -34,6 +35,8 @@ struct CompressArgs {
     const uint4 *wf;   // W_ft
     uint8_t *bits;     // one byte per chunk
     double *partials;  // [rows * segs]
+    float *alpha;      // written here directly when a row is one segment (segs == 1)
+    double count;      // elements per row: alpha = sum / count
     int64_t row_chunks;
     int64_t segs;
 };
@@ -59,17 +62,23 @@ __device__ __forceinline__ uint32_t chunk_signs(const uint4 &b, const uint4 &f, 
 }
 
 // Pass 1, persistent: CTA b walks segments b, b+G, b+2G, ... (2 CTAs per SM).
-// A producer warp streams each segment's W_base and W_ft bytes, half a
-// segment (1024 chunks, 32 KB) per ring slot, into a 3-slot shared-memory
-// ring with 1-D bulk copies; 256 consumer threads take chunk tid + 256u
-// (u = 0..7) of the segment.  A thread's eight chunk sums (fp32, pairwise over
-// 8 elements) are added pairwise in fp32, widened to fp64 and reduced with
-// xor-shuffles and across warps in a fixed order.  The assignment and order do
-// not depend on the grid, so each segment's partial (and alpha) is the same on
-// any device.  Worst-case relative error of a thread's fp32 sum: 6 levels of
-// pairwise rounding plus the fp32 subtraction, ~7 * 2^-24 < 5e-7.
+// A producer warp streams each segment's W_base and W_ft bytes (1024 chunks,
+// 16 KB per tensor: one ring slot) into a 3-slot shared-memory ring with 1-D
+// bulk copies; 256 consumer threads take chunk tid + 256u (u = 0..3) of the
+// segment.  A thread's four chunk sums (fp32, pairwise over 8 elements) are
+// added pairwise in fp32, widened to fp64 and reduced with xor-shuffles and
+// across warps in a fixed order.  The assignment and order do not depend on
+// the grid, so each segment's partial (and alpha) is the same on any device.
+// Worst-case relative error of a thread's fp32 sum: 5 levels of pairwise
+// rounding plus the fp32 subtraction, ~6 * 2^-24 < 5e-7.  Segments of 1024
+// chunks spread a matrix evenly over the persistent CTAs (a 4096 x 4096 scalar
+// compression has 2048 segments: at most 7 per CTA against 6.7 on average).
 constexpr int kRingStages = 3;
-constexpr int kHalfChunks = kCompressChunksPerSeg / 2;
+constexpr int kHalfChunks = 1024;                                          // chunks per ring slot
+constexpr int kSlotsPerSeg = static_cast<int>(kCompressChunksPerSeg / kHalfChunks);
+constexpr int kChunksPerSlotThread = kCompressChunksPerThread / kSlotsPerSeg;
+static_assert(kSlotsPerSeg * kHalfChunks == kCompressChunksPerSeg, "a segment is whole ring slots");
+static_assert(kChunksPerSlotThread * kCompressThreads == kHalfChunks, "a slot is whole chunks per thread");
 constexpr uint32_t kHalfBytes = static_cast<uint32_t>(kHalfChunks) * 16;  // per tensor
 constexpr int kPass1Threads = kCompressThreads + 32;
 constexpr size_t kPass1Smem = 128 + kRingStages * 2 * kHalfBytes + 256;
@@ -157,15 +166,16 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
             const uint4 *sb = reinterpret_cast<const uint4 *>(smem + st * 2 * kHalfBytes);
             const uint4 *sf = reinterpret_cast<const uint4 *>(smem + st * 2 * kHalfBytes + kHalfBytes);
 #pragma unroll
-            for (int uu = 0; uu < kCompressChunksPerThread / 2; ++uu) {
-                const int cl = uu * kCompressThreads + tid;        // chunk within this half
+            for (int uu = 0; uu < kChunksPerSlotThread; ++uu) {
+                const int cl = uu * kCompressThreads + tid;        // chunk within this slot
                 const int c = h * kHalfChunks + cl;                // chunk within the segment
                 if (c < n) {
                     float sum;
                     const uint32_t byte = chunk_signs(sb[cl], sf[cl], sum);
                     bits[c] = static_cast<uint8_t>(byte);
-                    if (h == 0) cs[uu] = sum;
-                    else cs[uu + kCompressChunksPerThread / 2] = sum;
+#pragma unroll
+                    for (int hh = 0; hh < kSlotsPerSeg; ++hh)
+                        if (h == hh) cs[hh * kChunksPerSlotThread + uu] = sum;
                 }
             }
             __syncwarp();
@@ -173,7 +183,11 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
         }
         // all consumer warps leave together on a timeout: the barrier below counts them all
         ok = __all_sync(0xFFFFFFFFu, ok);
-        const float t32 = ((cs[0] + cs[1]) + (cs[2] + cs[3])) + ((cs[4] + cs[5]) + (cs[6] + cs[7]));
+        float t32;
+        if constexpr (kCompressChunksPerThread == 8)
+            t32 = ((cs[0] + cs[1]) + (cs[2] + cs[3])) + ((cs[4] + cs[5]) + (cs[6] + cs[7]));
+        else
+            t32 = (cs[0] + cs[1]) + (cs[2] + cs[3]);
         double acc = static_cast<double>(t32);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
@@ -184,15 +198,23 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
             double s = 0.0;
 #pragma unroll
             for (int w = 0; w < kCompressThreads / 32; ++w) s += ws[w];
-            a.partials[sg] = s;
+            if (a.segs == 1)
+                a.alpha[row] = static_cast<float>(s / a.count);  // the row's only partial: no second pass
+            else
+                a.partials[sg] = s;
         }
         if (*abort_flag) break;
     }
 }
 
+// Pass 2 is launched as a programmatic dependent of pass 1: its CTAs become
+// resident while pass 1 streams and wait (griddepcontrol.wait) until pass 1
+// has completed and its partials are visible.
+
 // One thread per row (few segments per row): alpha_j = sum(partials)/count.
 __global__ void compress_pass2_rows(const double *partials, int64_t rows, int64_t segs, double count,
                                     float *alpha) {
+    pdl_trigger_and_wait();
     const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (r >= rows) return;
     double s = 0.0;
@@ -203,6 +225,7 @@ __global__ void compress_pass2_rows(const double *partials, int64_t rows, int64_
 // One block per row (many segments): strided per-thread sums, then a fixed tree.
 __global__ void __launch_bounds__(256) compress_pass2_block(const double *partials, int64_t segs, double count,
                                                             float *alpha) {
+    pdl_trigger_and_wait();
     const int64_t r = blockIdx.x;
     double s = 0.0;
     for (int64_t i = threadIdx.x; i < segs; i += 256) s += partials[r * segs + i];
@@ -240,6 +263,8 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
     a.wf = static_cast<const uint4 *>(w_ft);
     a.bits = bits;
     a.partials = partials;
+    a.alpha = alpha;
+    a.count = static_cast<double>(g.row_chunks) * 8.0;
     a.row_chunks = g.row_chunks;
     a.segs = g.segs;
     const int64_t n_segs = g.rows * g.segs;
@@ -262,15 +287,21 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, compress_pass1, a, n_segs, ctx.status, ctx.wait_ns);
-    if (e != cudaSuccess) return e;
-    const double count = static_cast<double>(g.row_chunks) * 8.0;
+    if (e != cudaSuccess || g.segs == 1) return e;  // one segment per row: pass 1 wrote alpha
+    const double count = a.count;
+    cudaLaunchConfig_t c2 = {};
+    c2.stream = stream;
+    c2.attrs = attr;
+    c2.numAttrs = 1;
     if (g.segs <= 32) {
-        const int64_t nb = (g.rows + 127) / 128;
-        compress_pass2_rows<<<static_cast<unsigned>(nb), 128, 0, stream>>>(partials, g.rows, g.segs, count, alpha);
-    } else {
-        compress_pass2_block<<<static_cast<unsigned>(g.rows), 256, 0, stream>>>(partials, g.segs, count, alpha);
+        c2.gridDim = dim3(static_cast<unsigned>((g.rows + 127) / 128), 1, 1);
+        c2.blockDim = dim3(128, 1, 1);
+        return cudaLaunchKernelEx(&c2, compress_pass2_rows, static_cast<const double *>(partials), g.rows, g.segs,
+                                  count, alpha);
     }
-    return cudaGetLastError();
+    c2.gridDim = dim3(static_cast<unsigned>(g.rows), 1, 1);
+    c2.blockDim = dim3(256, 1, 1);
+    return cudaLaunchKernelEx(&c2, compress_pass2_block, static_cast<const double *>(partials), g.segs, count, alpha);
 }
 
 }  // namespace bd

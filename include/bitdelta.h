@@ -78,7 +78,7 @@ typedef enum bd_alpha_mode {
  * fp32 from the bf16 inputs).  Writes the packed sign bits and alpha:
  *   scalar:  alpha[0] = sum_{j,k} |Delta_jk| / (n_out * n_in)
  *   per-row: alpha[j] = sum_k |Delta_jk| / n_in
- * The sums use pairwise fp32 partials over at most 64 elements, widened to
+ * The sums use pairwise fp32 partials over at most 32 elements, widened to
  * fp64 and reduced in a fixed order (relative error below 5e-7), so alpha is
  * bitwise reproducible for a given shape, and is rounded once to fp32.
  *
@@ -110,8 +110,8 @@ int32_t bd_compress(const void *w_base, const void *w_ft, int64_t n_out,
  * the partial sums live in a fixed scratch array built into the library,
  * BD_NOALLOC_MAX_PARTIALS doubles (1 MiB) per GPU that loads the library,
  * held until the process exits.  A shape fits when
- *   rows * ceil(chunks / 2048) <= BD_NOALLOC_MAX_PARTIALS,
- * with rows = 1 and chunks = n_out*n_in/8 for a scalar alpha (up to 2^31
+ *   rows * ceil(chunks / 1024) <= BD_NOALLOC_MAX_PARTIALS,
+ * with rows = 1 and chunks = n_out*n_in/8 for a scalar alpha (up to 2^30
  * elements), or rows = n_out and chunks = n_in/8 per row; larger shapes
  * return BD_ERR_WORKSPACE before launching anything (use bd_compress).
  * The call allocates and frees nothing.  Its first call on a device looks

@@ -54,11 +54,11 @@ def test_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # scalar alpha: one fp64 partial per 2048 chunks of 8 elements
-    assert bd.bd_compress_workspace_size(256, 512, 0) == (256 * 64 // 2048) * 8
-    assert bd.bd_compress_workspace_size(4096, 4096, 0) == (4096 * 512 // 2048) * 8
-    # per-row alpha: rows * segments per row
-    assert bd.bd_compress_workspace_size(8192, 28672, 1) == 8192 * 2 * 8
+    # scalar alpha: one fp64 partial per 1024 chunks of 8 elements
+    assert bd.bd_compress_workspace_size(256, 512, 0) == (256 * 64 // 1024) * 8
+    assert bd.bd_compress_workspace_size(4096, 4096, 0) == (4096 * 512 // 1024) * 8
+    # per-row alpha: rows * segments per row (28672 / 8 = 3584 chunks -> 4 segments)
+    assert bd.bd_compress_workspace_size(8192, 28672, 1) == 8192 * 4 * 8
     assert bd.bd_compress_workspace_size(4, 12, 0) == 0          # n_in not a multiple of 8
     assert bd.bd_compress_workspace_size(4, 16, 5) == 0          # unknown mode
     assert bd.bd_linear_grouped_workspace_size(64, 14, 8192, 8192) > 64 * 8192 * 2
