@@ -609,7 +609,8 @@ class _NoLib:
 def run_kernel_case(args):
     """One kernel on one shape, launched eagerly (no graph): for ncu captures and sweeps.
 
-    --kernel-case linear:N_OUTxN_IN:M[:path]  or  compress:N_OUTxN_IN[:mode]
+    --kernel-case linear:N_OUTxN_IN:M[:path], compress:N_OUTxN_IN[:mode] or
+                  grouped:N_OUTxN_IN:M:V (V variants, uniform ids)
     Rotates over enough copies of the weights that the working set exceeds L2.
     """
     from bit_delta_tenant_gb300 import build as lib_build
@@ -644,6 +645,28 @@ def run_kernel_case(args):
         def call(i):
             bd.bd_linear(x, mats[i][0], packed[i][0], packed[i][1], 0, y)
         work = decode_bytes(m, n_out, n_in, 0)
+        flops = 2.0 * m * n_out * n_in
+    elif kind == "grouped":
+        m, nv = int(parts[2]), int(parts[3])
+        bd.bd_set_weight_prefetch(0)
+        packed = []
+        for i, (wb, wf) in enumerate(mats):
+            vs = []
+            for v in range(nv):
+                g = synth.generator(900 + 31 * i + v, dev)
+                bits = torch.randint(0, 256, (n_out, n_in // 8), generator=g, device=dev, dtype=torch.uint8)
+                vs.append((bits, torch.full((1,), 1e-3, dtype=torch.float32, device=dev)))
+            packed.append(vs)
+        ids = torch.from_numpy(synth.uniform_ids(m, nv, 3)).to(dev)
+        x = synth.activations(m, n_in, 7, dev)
+        y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+        gws = torch.empty((bd.bd_linear_grouped_workspace_size(m, nv, n_out, n_in),), dtype=torch.uint8, device=dev)
+
+        def call(i):
+            bd.bd_linear_grouped(x, ids, mats[i][0], [b for b, _ in packed[i]], [a for _, a in packed[i]],
+                                 [0] * nv, y, gws)
+        active = len(set(ids.tolist()))
+        work = 2.0 * n_out * n_in + active * n_out * n_in / 8 + 4.0 * nv + 2.0 * m * n_in + 2.0 * m * n_out
         flops = 2.0 * m * n_out * n_in
     else:
         mode = int(parts[2]) if len(parts) > 2 else 0

@@ -18,8 +18,8 @@
 // owns 16-byte chunks (8 bf16) of both inputs, so one chunk yields exactly one
 // output byte in registers with no cross-lane exchange, and lanes own
 // consecutive chunks, so the byte stores are 32-byte coalesced.  |Delta| is
-// summed pairwise in fp32 per thread (32 terms), widened to fp64, reduced
-// through the warp with xor-shuffles and across warps in a fixed order: one
+// summed pairwise in fp32 per thread (32 terms), reduced through the warp with
+// xor-shuffles in double-float and across warps in fp64, in a fixed order: one
 // fp64 partial per 1024-chunk segment.  A second kernel adds each row's
 // partials in a fixed order and rounds alpha to fp32 once, so alpha is bitwise
 // reproducible for a given shape on any device; a row that is a single
@@ -61,13 +61,25 @@ __device__ __forceinline__ uint32_t chunk_signs(const uint4 &b, const uint4 &f, 
     return byte;
 }
 
+// (hi, lo) += (bhi, blo) in double-float arithmetic: TwoSum (Knuth) gives the
+// exact rounding error of hi + bhi, the low parts join it, and a FastTwoSum
+// renormalises.  Plain fp32 adds only (no multiplies, so nothing contracts).
+__device__ __forceinline__ void df_add(float &hi, float &lo, float bhi, float blo) {
+    const float s = __fadd_rn(hi, bhi);
+    const float bb = __fsub_rn(s, hi);
+    const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(bhi, bb));
+    const float e = __fadd_rn(__fadd_rn(err, lo), blo);
+    hi = __fadd_rn(s, e);
+    lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
 // Pass 1, persistent: CTA b walks segments b, b+G, b+2G, ... (2 CTAs per SM).
 // A producer warp streams each segment's W_base and W_ft bytes (1024 chunks,
 // 16 KB per tensor: one ring slot) into a 3-slot shared-memory ring with 1-D
 // bulk copies; 256 consumer threads take chunk tid + 256u (u = 0..3) of the
 // segment.  A thread's four chunk sums (fp32, pairwise over 8 elements) are
-// added pairwise in fp32, widened to fp64 and reduced with xor-shuffles and
-// across warps in a fixed order.  The assignment and order do not depend on
+// added pairwise in fp32 and reduced with xor-shuffles in double-float (fp32
+// pairs), then across warps in fp64, in a fixed order.  The assignment and order do not depend on
 // the grid, so each segment's partial (and alpha) is the same on any device.
 // Worst-case relative error of a thread's fp32 sum: 5 levels of pairwise
 // rounding plus the fp32 subtraction, ~6 * 2^-24 < 5e-7.  Segments of 1024
@@ -188,11 +200,19 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
             t32 = ((cs[0] + cs[1]) + (cs[2] + cs[3])) + ((cs[4] + cs[5]) + (cs[6] + cs[7]));
         else
             t32 = (cs[0] + cs[1]) + (cs[2] + cs[3]);
-        double acc = static_cast<double>(t32);
+        // Warp tree in double-float (an fp32 pair, ~44 significant bits): GB300
+        // runs fp64 at a small fraction of the fp32 rate, so only the per-warp
+        // results are widened.  Lane 0's operand order is fixed, so its result is
+        // the same on every run.
+        float hi = t32, lo = 0.0f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, off);
+            const float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, off);
+            df_add(hi, lo, ohi, olo);
+        }
         double *ws = warp_sum + (seg_i & 1) * 8;
-        if (lane == 0) ws[warp] = acc;
+        if (lane == 0) ws[warp] = static_cast<double>(hi) + static_cast<double>(lo);
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (!*abort_flag && tid == 0) {
             double s = 0.0;
