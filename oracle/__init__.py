@@ -66,6 +66,7 @@ def _load():
         lib.bdo_alpha.argtypes = [P, P, I64, I64, ctypes.c_int, P]
         lib.bdo_unpack_signs.argtypes = [P, I64, I64, P]
         lib.bdo_weff.argtypes = [P, P, P, ctypes.c_int, I64, I64, P]
+        lib.bdo_weff_bf16.argtypes = [P, P, P, ctypes.c_int, I64, I64, P]
         lib.bdo_linear.argtypes = [P, I64, P, P, P, ctypes.c_int, I64, I64, P, P]
         lib.bdo_linear_sampled.argtypes = [P, P, P, P, ctypes.c_int, I64, I64, P, P, I64, P, P]
         lib.bdo_linear_grouped.argtypes = [P, P, I64, P, P, P, P, I32, I64, I64, P, P]
@@ -148,6 +149,17 @@ def w_eff(w_base: np.ndarray, bits: np.ndarray, alpha32: np.ndarray, mode: int) 
     a = _c(alpha32, np.float32)
     out = np.empty((n_out, n_in), np.float64)
     _load().bdo_weff(_p(wb), _p(b), _p(a), int(mode), n_out, n_in, _p(out))
+    return out
+
+
+def w_eff_bf16(w_base: np.ndarray, bits: np.ndarray, alpha32: np.ndarray, mode: int) -> np.ndarray:
+    """bf16 bit patterns of W_eff formed in fp32 and rounded once to nearest even (reading R5)."""
+    wb = _c(w_base, np.uint16)
+    n_out, n_in = wb.shape
+    b = _c(bits, np.uint8)
+    a = _c(alpha32, np.float32)
+    out = np.empty((n_out, n_in), np.uint16)
+    _load().bdo_weff_bf16(_p(wb), _p(b), _p(a), int(mode), n_out, n_in, _p(out))
     return out
 
 

@@ -25,7 +25,9 @@
  *   - "int8" storage is read as raw bytes (uint8 here, so shifts never sign
  *     extend); the byte values are identical.
  *
- * All arithmetic is fp64.  bf16 inputs arrive as their 16-bit patterns
+ * All arithmetic is fp64, except bdo_weff_bf16, which produces the stored
+ * bf16 W_eff and therefore takes the rounding decisions the reading fixes
+ * (fp32 sum, one rounding to bf16).  bf16 inputs arrive as their 16-bit patterns
  * (uint16) and widen exactly.  Sums are plain left-to-right loops: no
  * blocking, no reassociation.  Rows of independent outputs may run on
  * separate OpenMP threads; that changes no sum.
@@ -136,6 +138,38 @@ void bdo_weff(const uint16_t *w_base, const uint8_t *bits, const float *alpha,
         for (int64_t k = 0; k < n_in; ++k)
             w_eff[j * n_in + k] =
                 bf16_to_f64(w_base[j * n_in + k]) + a * sign_at(bits, bpr, j, k);
+    }
+}
+
+/* Round an fp32 value to the nearest bf16, ties to the even significand (the
+ * standard IEEE rounding, done on the bit pattern: add just under half an
+ * ulp of the kept part, plus its lowest kept bit, and truncate).  Finite
+ * inputs only, which is all this file produces. */
+static uint16_t f32_to_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* [serve] with reading R5: the bf16 W_eff a standard matmul would consume
+ * ("Profil de latence" reads decode as a standard matmul).  The sum
+ * W_base + alpha * sign is formed in fp32 (alpha * (+-1) is exact, the add
+ * rounds once to nearest even) and then rounded once, to nearest even, to
+ * bf16. */
+void bdo_weff_bf16(const uint16_t *w_base, const uint8_t *bits, const float *alpha,
+                   int mode, int64_t n_out, int64_t n_in, uint16_t *w_eff)
+{
+    const int64_t bpr = n_in / 8;
+    for (int64_t j = 0; j < n_out; ++j) {
+        const float a = mode == 1 ? alpha[j] : alpha[0];
+        for (int64_t k = 0; k < n_in; ++k) {
+            const float w = (float)bf16_to_f64(w_base[j * n_in + k]);
+            const float s = (float)sign_at(bits, bpr, j, k);
+            const float v = w + a * s;
+            w_eff[j * n_in + k] = f32_to_bf16_rne(v);
+        }
     }
 }
 

@@ -301,3 +301,45 @@ def test_storage_arithmetic_matches_printed_figures():
     for n_out, n_in in [(4096, 4096), (11008, 4096), (3, 24)]:
         assert oracle.packed_bytes(n_out, n_in) / (n_out * n_in * 4) == printed["fraction_of_fp32_delta"]
         assert oracle.packed_bytes(n_out, n_in) * 16 == n_out * n_in * 2   # 1/16 of a bf16 delta
+
+
+def _weff_cases():
+    out = []
+    with open(os.path.join(GOLDEN, "weff_bf16.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, wb, a, sbit, exp = [p.strip() for p in line.split(";")]
+            out.append((name, int(wb, 16), float(a), int(sbit), int(exp, 16)))
+    return out
+
+
+@pytest.mark.parametrize("case", _weff_cases(), ids=lambda c: c[0])
+def test_weff_bf16_hand_worked_rounding(case):
+    name, wb, a, sbit, exp = case
+    w = np.array([[wb] * 8], np.uint16)
+    bits = np.array([[0xFF if sbit else 0x00]], np.uint8)
+    got = oracle.w_eff_bf16(w, bits, np.array([a], np.float32), 0)
+    assert np.all(got == exp), (name, [hex(v) for v in got[0]], hex(exp))
+
+
+def test_weff_bf16_special_cases_and_half_ulp_bound():
+    wb, wf = synth.matrix_pair(64, 256, 0.02, 1e-3, seed=11)
+    wb_h, wf_h = synth.as_u16(wb), synth.as_u16(wf)
+    bits, a32, _ = oracle.compress(wb_h, wf_h, 0)
+    # alpha = 0: W_eff is W_base itself (the base has no -0.0 entries, which +0.0 would turn into +0.0)
+    assert not np.any(wb_h == 0x8000)
+    assert np.array_equal(oracle.w_eff_bf16(wb_h, bits, np.zeros(1, np.float32), 0), wb_h)
+    # W_base = 0, alpha exact in bf16: W_eff = +-alpha exactly
+    z = np.zeros_like(wb_h)
+    alpha_exact = np.array([0.0078125], np.float32)
+    s = oracle.unpack_signs(bits, 256).astype(np.float64)
+    got = _bf16_to_f64(oracle.w_eff_bf16(z, bits, alpha_exact, 0))
+    assert np.array_equal(got, 0.0078125 * s)
+    # general case, per-row alpha: within half a bf16 ulp of the exact fp64 W_eff
+    bits1, a1, _ = oracle.compress(wb_h, wf_h, 1)
+    exact = oracle.w_eff(wb_h, bits1, a1, 1)
+    got = _bf16_to_f64(oracle.w_eff_bf16(wb_h, bits1, a1, 1))
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(exact))) - 7)
+    assert np.all(np.abs(got - exact) <= 0.5 * ulp * (1 + 2.0 ** -16))
