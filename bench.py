@@ -609,8 +609,9 @@ class _NoLib:
 def run_kernel_case(args):
     """One kernel on one shape, launched eagerly (no graph): for ncu captures and sweeps.
 
-    --kernel-case linear:N_OUTxN_IN:M[:path], compress:N_OUTxN_IN[:mode] or
-                  grouped:N_OUTxN_IN:M:V (V variants, uniform ids)
+    --kernel-case linear:N_OUTxN_IN:M[:path], compress:N_OUTxN_IN[:mode],
+                  grouped:N_OUTxN_IN:M:V (V variants, uniform ids), reconstruct:N_OUTxN_IN
+                  (W_eff materialised) or reconstruct_mm:N_OUTxN_IN:M (W_eff + a cuBLAS matmul)
     Rotates over enough copies of the weights that the working set exceeds L2.
     """
     from bit_delta_tenant_gb300 import build as lib_build
@@ -645,6 +646,30 @@ def run_kernel_case(args):
         def call(i):
             bd.bd_linear(x, mats[i][0], packed[i][0], packed[i][1], 0, y)
         work = decode_bytes(m, n_out, n_in, 0)
+        flops = 2.0 * m * n_out * n_in
+    elif kind in ("reconstruct", "reconstruct_mm"):
+        # the page's "standard matmul in decode" reading: rebuild W_eff in HBM (and,
+        # for reconstruct_mm, multiply with a cuBLAS GEMM); compare with linear:...
+        m = int(parts[2]) if kind == "reconstruct_mm" else 0
+        packed = []
+        for wb, wf in mats:
+            bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=dev)
+            alpha = torch.empty((1,), dtype=torch.float32, device=dev)
+            ws = torch.empty((max(16, bd.bd_compress_workspace_size(n_out, n_in, 0)),), dtype=torch.uint8,
+                             device=dev)
+            bd.bd_compress(wb, wf, 0, bits, alpha, ws)
+            packed.append((bits, alpha))
+        torch.cuda.synchronize()
+        w_eff = torch.empty((n_out, n_in), dtype=torch.bfloat16, device=dev)
+        x = synth.activations(max(m, 1), n_in, 7, dev)
+        y = torch.empty((max(m, 1), n_out), dtype=torch.bfloat16, device=dev)
+
+        def call(i):
+            bd.bd_reconstruct(mats[i][0], packed[i][0], packed[i][1], 0, w_eff)
+            if m:
+                torch.matmul(x, w_eff.t(), out=y)
+        # reconstruct alone: its own traffic; with the matmul: the fused linear's algorithmic bytes
+        work = decode_bytes(m, n_out, n_in, 0) if m else 4.0 * n_out * n_in + n_out * n_in / 8
         flops = 2.0 * m * n_out * n_in
     elif kind == "grouped":
         m, nv = int(parts[2]), int(parts[3])

@@ -59,6 +59,8 @@ def load_library(path: str | None = None):
         lib.bd_set_wait_limit_ns.restype = I64
         lib.bd_set_linear_path.argtypes = [I32]
         lib.bd_set_linear_path.restype = I32
+        lib.bd_reconstruct.argtypes = [V, V, V, I32, I64, I64, V, V]
+        lib.bd_reconstruct.restype = I32
         lib.bd_set_weight_prefetch.argtypes = [I32]
         lib.bd_set_weight_prefetch.restype = I32
         lib.bd_get_device_status.argtypes = [V]
@@ -161,6 +163,15 @@ def bd_linear(x: torch.Tensor, w_base: torch.Tensor, bits: torch.Tensor, alpha: 
 
 def bd_linear_grouped_workspace_size(m: int, n_variants: int, n_out: int, n_in: int) -> int:
     return int(load_library().bd_linear_grouped_workspace_size(m, n_variants, n_out, n_in))
+
+
+def bd_reconstruct(w_base: torch.Tensor, bits: torch.Tensor, alpha: torch.Tensor, alpha_mode: int,
+                   w_eff: torch.Tensor, stream=None) -> None:
+    """W_eff = bf16(W_base + alpha * s), materialised (for a standard matmul)."""
+    n_out, n_in = w_base.shape
+    rc = load_library().bd_reconstruct(_ptr(w_base), _ptr(bits), _ptr(alpha), int(alpha_mode), n_out, n_in,
+                                       _ptr(w_eff), _stream(stream))
+    _check(rc, "bd_reconstruct")
 
 
 def bd_linear_grouped(x: torch.Tensor, variant_ids: torch.Tensor, w_base: torch.Tensor, bits_v, alpha_v,

@@ -231,6 +231,20 @@ BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uin
     return cuda_status(bd::launch_prefill(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));
 }
 
+BD_API int32_t bd_reconstruct(const void *w_base, const uint8_t *bits, const float *alpha, int32_t alpha_mode,
+                              int64_t n_out, int64_t n_in, void *w_eff, void *stream) {
+    if (!w_base || !bits || !alpha || !w_eff) return BD_ERR_INVALID_ARG;
+    if (alpha_mode != BD_ALPHA_SCALAR && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    const int32_t shape = check_matrix_shape(n_out, n_in);
+    if (shape != BD_OK) return shape;
+    if (!aligned16(w_base) || !aligned16(bits) || !aligned16(alpha) || !aligned16(w_eff)) return BD_ERR_MISALIGNED;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    return cuda_status(bd::launch_reconstruct(w_base, bits, alpha, alpha_mode, n_out, n_in, w_eff, ctx,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 // ---------------------------------------------------------------- multi-tenant
 
 BD_API size_t bd_linear_grouped_workspace_size(int64_t m, int32_t n_variants, int64_t n_out, int64_t n_in) {

@@ -53,6 +53,10 @@ cudaError_t launch_decode(const void *x, int64_t m, const void *w_base, const ui
                           int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                           cudaStream_t stream);
 
+// W_eff = bf16(fp32(W_base) + alpha * s) materialised in HBM (for a standard matmul).
+cudaError_t launch_reconstruct(const void *w_base, const uint8_t *bits, const float *alpha, int32_t alpha_mode,
+                               int64_t n_out, int64_t n_in, void *w_eff, const DevCtx &ctx, cudaStream_t stream);
+
 // TMA-fed variant of the streaming kernel (n_in % 128 == 0, 16-byte aligned
 // W_base and bits); preferred whenever it applies.
 bool decode_tma_supported(int64_t m, int64_t n_out, int64_t n_in, const void *w_base, const uint8_t *bits,

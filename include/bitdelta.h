@@ -151,6 +151,29 @@ int32_t bd_linear(const void *x, int64_t m, const void *w_base,
                   int64_t n_out, int64_t n_in, void *y, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * Reconstruct-only pass ([serve]: W_eff = W_base + alpha * unpacked signs,
+ * then a plain linear; [latency] reads decode as a standard matmul)
+ *
+ *   w_eff[j, k] = bf16_rn( fp32(W_base[j, k]) + alpha_(j) * s_jk )
+ * with the fp32 add rounded to nearest even and the result rounded once, to
+ * nearest even, to bf16 -- the bf16 weight a standard GEMM would consume.
+ * Provided to measure that reading against the fused path (which never
+ * writes W_eff); the fused path is the one to use.
+ *
+ *   w_base  bf16 [n_out, n_in]   (read)
+ *   bits    uint8 [n_out, n_in/8] (read)
+ *   alpha   float [1] or [n_out] (read)
+ *   w_eff   bf16 [n_out, n_in]   (written; may not alias the inputs)
+ * All device pointers, 16-byte aligned; caller-owned.  Ordered on `stream`.
+ * Errors: BD_ERR_INVALID_ARG (null pointer, bad mode, empty shape),
+ *         BD_ERR_UNSUPPORTED_SHAPE (n_in % 8 != 0 or a dimension >=
+ *         BD_MAX_DIM), BD_ERR_MISALIGNED, BD_ERR_CUDA (launch failure).
+ * ------------------------------------------------------------------------ */
+int32_t bd_reconstruct(const void *w_base, const uint8_t *bits, const float *alpha,
+                       int32_t alpha_mode, int64_t n_out, int64_t n_in,
+                       void *w_eff, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Multi-tenant fused linear  ([serve]: many fine-tuned variants share one
  * resident W_base; each request uses its own variant's packed delta)
  *

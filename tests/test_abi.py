@@ -134,3 +134,14 @@ def test_knobs_round_trip(lib):
     w = bd.bd_set_weight_prefetch(1)
     assert bd.bd_set_weight_prefetch(7) == 1          # any non-zero value enables
     assert bd.bd_set_weight_prefetch(w) == 1
+
+
+def test_reconstruct_rejects_bad_arguments(lib):
+    def rc(wb=ALIGNED, bits=ALIGNED, alpha=ALIGNED, mode=0, n_out=4, n_in=16, out=ALIGNED):
+        return lib.bd_reconstruct(wb, bits, alpha, mode, n_out, n_in, out, None)
+    assert rc(wb=0) == bd.BD_ERR_INVALID_ARG
+    assert rc(out=0) == bd.BD_ERR_INVALID_ARG
+    assert rc(mode=2) == bd.BD_ERR_INVALID_ARG
+    assert rc(n_out=0) == bd.BD_ERR_INVALID_ARG
+    assert rc(n_in=12) == bd.BD_ERR_UNSUPPORTED_SHAPE
+    assert rc(out=ALIGNED + 8) == bd.BD_ERR_MISALIGNED
