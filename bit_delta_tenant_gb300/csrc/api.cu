@@ -214,7 +214,7 @@ BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uin
     const int32_t path = g_linear_path.load();
     const bool tma_ok = bd::decode_tma_supported(m, n_out, n_in, w_base, bits, ctx);
     const bool decode_ok = tma_ok || bd::decode_supported(m, n_out, n_in, ctx.num_sms);
-    bool use_decode = decode_ok && m <= bd::kDecodeMaxM;
+    bool use_decode = decode_ok && m <= bd::kAutoStreamMaxM;
     if (path == 1) {
         if (!decode_ok) return BD_ERR_UNSUPPORTED_SHAPE;
         use_decode = true;

@@ -13,13 +13,14 @@
 //   warp 0      TMA producer: per 64-wide K block, the W_base tile
 //               [128 x 64] and the x tile [256 x 64], both K-major with the
 //               128-byte swizzle, into a 4-stage ring.
-//   warps 2..9  reconstruction: two threads per tile row, each with half of
-//               the row's 8 packed bytes for the K block (prefetched two
-//               blocks ahead); each rebuilds its four 16-byte chunks of the
-//               swizzled W tile as bf16(fp32(W_base) + alpha_r * s) -- one
-//               chunk is exactly one packed byte.  After the K loop the same
-//               warps are the epilogue (warp w reads TMEM lanes 32*(w%4)..+31,
-//               two warps per lane quarter splitting the token columns).
+//   warps 2..9  reconstruction, in two groups of four that take alternate K
+//               blocks (so two blocks are rebuilt at once): one thread per tile
+//               row, with the row's 8 packed bytes of the block (prefetched
+//               three of its blocks ahead); it rebuilds the row's eight 16-byte
+//               chunks of the swizzled W tile as bf16(fp32(W_base) + alpha_r*s)
+//               -- one chunk is exactly one packed byte.  After the K loop the
+//               same warps are the epilogue (warp w reads TMEM lanes
+//               32*(w%4)..+31, the two groups splitting the token columns).
 //   warp 1      allocates TMEM (256 accumulator columns, plus 32 columns per
 //               stage for the rebuilt A tile); lane 0 issues tcgen05.mma
 //               kind::f16 (M=128, N=tokens<=256, K=16, bf16 in, fp32
@@ -28,28 +29,41 @@
 // MMA takes A from there, so shared memory carries only the TMA fills, the
 // rebuild reads and the activation (B) operand; with BD_PREFILL_TMEM_A=0 the
 // tile is instead written back in place and read by the MMA from shared memory.
+// When the output tiles alone would leave SMs idle (small m or few W rows), a
+// cluster of C CTAs shares one output tile, each rank covering K/C: after the
+// last MMA every rank parks its fp32 tile in its (now idle) ring memory and the
+// cluster adds the C tiles in rank order through distributed shared memory.
 // Every wait is bounded; a role that gives up records a timeout in the status
 // word, tells the other roles through a shared flag, drains its own copies
 // and MMAs in flight, and the CTA frees its TMEM and returns.
+#include <cooperative_groups.h>
+
 #include <cstdlib>
 
 #include "bd_device.cuh"
 #include "bd_internal.h"
 
+namespace cg = cooperative_groups;
+
 namespace bd {
 namespace {
 
 constexpr int kBM = 128;  // W rows per tile (MMA M)
-constexpr int kBN = 256;  // tokens per tile (MMA N)
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
 constexpr uint32_t kWBytes = kBM * kBK * 2;
-constexpr uint32_t kXBytes = kBN * kBK * 2;
-constexpr uint32_t kStageTx = kWBytes + kXBytes;
 constexpr int kRebuildWarps = 8;
 constexpr int kThreads = (2 + kRebuildWarps) * 32;  // producer, MMA issuer, rebuild/epilogue
-constexpr uint32_t kAccCols = 256;  // fp32 accumulator columns (one per token)
-constexpr size_t kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 256;
+
+// Token tile BN (MMA N): 256 for prefill; 64 for m <= 64, whose smaller
+// activation tile leaves room for a ring twice as deep (more W in flight).
+template <int BN>
+struct Tile {
+    static constexpr int kStages = BN >= 256 ? 4 : 8;
+    static constexpr uint32_t kXBytes = BN * kBK * 2;
+    static constexpr uint32_t kStageTx = kWBytes + kXBytes;
+    static constexpr uint32_t kAccCols = BN;  // fp32 accumulator columns (one per token)
+    static constexpr size_t kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 256;
+};
 constexpr int kMaxVariants = 64;
 
 struct PrefillArgs {
@@ -60,6 +74,8 @@ struct PrefillArgs {
     int32_t mode;
     int32_t num_kb;
     int32_t row_tiles, tok_tiles, group;
+    int32_t ksplit;     // ranks of a cluster splitting K (1: no split)
+    int32_t kb_per;     // K blocks per rank
     int32_t bits_vec8;  // rows of packed bits are 8-byte aligned
     unsigned *status;
     uint64_t wait_ns;
@@ -91,14 +107,20 @@ __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *stat
     flag_status(status, kDevTimeout);
 }
 
-template <bool kGrouped, bool kTmemA>
+template <bool kGrouped, bool kTmemA, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                    const __grid_constant__ PrefillArgs a) {
+    constexpr int kBN = BN;
+    constexpr int kStages = Tile<BN>::kStages;
+    constexpr uint32_t kXBytes = Tile<BN>::kXBytes;
+    constexpr uint32_t kStageTx = Tile<BN>::kStageTx;
+    constexpr uint32_t kAccCols = Tile<BN>::kAccCols;
     extern __shared__ uint8_t smem_raw[];
     // With kTmemA the rebuilt W tile goes to tensor memory (columns 256 + 32*stage)
     // and the MMA reads A from there; otherwise it is written back in place.
-    constexpr uint32_t kTmemCols = kTmemA ? 512 : 256;
+    constexpr uint32_t kTmemCols = kTmemA ? 512 : (BN < 32 ? 32 : BN);
+    static_assert(!kTmemA || kAccCols + kStages * (kBK / 2) <= 512, "accumulator + A buffers fit in TMEM");
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;
     uint8_t *sX = smem + kStages * kWBytes;
@@ -130,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // Grouped rasterisation: consecutive CTAs cycle over `group` token tiles
         // for one W tile, so a wave touches a compact block of W and x in L2.
-        const int tile = blockIdx.x;
+        const int tile = blockIdx.x / a.ksplit;  // the ranks of a cluster share one output tile
         const int per_group = a.group * a.row_tiles;
         const int grp = tile / per_group;
         const int rem = tile - grp * per_group;
@@ -149,12 +171,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nkb = a.num_kb;
+    // K blocks [kb0, kb0 + nkb) of this CTA (all of them unless a cluster splits K)
+    const int kb0 = kGrouped ? 0 : static_cast<int>(blockIdx.x % a.ksplit) * a.kb_per;
+    const int nkb = kGrouped ? a.num_kb : min(a.kb_per, a.num_kb - kb0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&rebuilt[s], kRebuildWarps);
+            mbar_init(&rebuilt[s], kRebuildWarps / 2);  // the warp group of the block's parity
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
@@ -183,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&full[s], kStageTx);
-                tma_load_2d(sW + s * kWBytes, &tm_w, &full[s], kb * kBK, m0);
-                tma_load_2d(sX + s * kXBytes, &tm_x, &full[s], kb * kBK, n0);
+                tma_load_2d(sW + s * kWBytes, &tm_w, &full[s], (kb0 + kb) * kBK, m0);
+                tma_load_2d(sX + s * kXBytes, &tm_x, &full[s], (kb0 + kb) * kBK, n0);
                 issued = kb + 1;
             }
             if (*abort_flag) {
@@ -227,12 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---- rebuild (then epilogue) warps ------------------------------------------
-        // Thread q owns tile row r = 32*(warp%4) + lane and chunk pair h (0..3):
-        // the 16-byte chunks 2h, 2h+1 of the row in every K block (two packed
-        // bytes).  Warp w may read TMEM lanes 32*(w%4)..+31 only, so the same
-        // row mapping serves the epilogue, where h picks a quarter of the tokens.
-        constexpr int kParts = kRebuildWarps / 4;        // threads per row
-        constexpr int kChunks = 8 / kParts;              // chunks per thread per K block
+        // Thread q of warp group h (warps 2..5: h = 0, warps 6..9: h = 1) owns tile
+        // row r = 32*(warp%4) + lane: all eight 16-byte chunks of the row (its 8
+        // packed bytes) in the K blocks of parity h, so the two groups rebuild
+        // consecutive blocks at the same time.  Warp w may read TMEM lanes
+        // 32*(w%4)..+31 only, so the same row mapping serves the epilogue, where h
+        // picks half of the tokens.
+        constexpr int kParts = 2;  // warp groups: K-block parity, then token half
         const int sub = warp & 3;
         const int h = (warp - 2) >> 2;
         const int r = sub * 32 + lane;
@@ -241,33 +266,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float al = row_ok ? (mode ? alpha[row] : alpha[0]) : 0.0f;
         const uint32_t neg_al = __float_as_uint(-al);
         const int64_t bpr = a.n_in / 8;
-        const uint8_t *brow = bits + (row_ok ? row : 0) * bpr + kChunks * h;
+        const uint8_t *brow = bits + (row_ok ? row : 0) * bpr;
 
-        auto load_bits = [&](int kb) -> uint32_t {
-            uint32_t v = 0;
-            if (row_ok && kb < nkb) {
-                const int64_t c0 = static_cast<int64_t>(kb) * 8 + kChunks * h;  // first packed byte
-                if (a.bits_vec8 && c0 + kChunks <= bpr) {
-                    const uint8_t *q = brow + static_cast<int64_t>(kb) * 8;
-                    if constexpr (kChunks == 4) v = __ldg(reinterpret_cast<const uint32_t *>(q));
-                    else if constexpr (kChunks == 2) v = __ldg(reinterpret_cast<const uint16_t *>(q));
-                    else v = __ldg(q);
+        auto load_bits = [&](int kbl) -> uint2 {  // kbl: this CTA's K block index
+            uint2 v = make_uint2(0u, 0u);
+            const int64_t c0 = static_cast<int64_t>(kb0 + kbl) * 8;  // first packed byte
+            if (row_ok && kbl < nkb) {
+                if (a.bits_vec8 && c0 + 8 <= bpr) {
+                    v = __ldg(reinterpret_cast<const uint2 *>(brow + c0));
                 } else {
-                    for (int c = 0; c < kChunks; ++c)
-                        if (c0 + c < bpr)
-                            v |= static_cast<uint32_t>(__ldg(brow + static_cast<int64_t>(kb) * 8 + c)) << (8 * c);
+                    for (int c = 0; c < 8; ++c)
+                        if (c0 + c < bpr) {
+                            const uint32_t byte = __ldg(brow + c0 + c);
+                            if (c < 4) v.x |= byte << (8 * c);
+                            else v.y |= byte << (8 * (c - 4));
+                        }
                 }
             }
             return v;
         };
 
-        uint32_t b_cur = load_bits(0);
-        uint32_t b_nxt = load_bits(1);
+        // Packed bits arrive by plain loads three of this group's K blocks ahead.
+        constexpr int kBitsAhead = 3;
+        uint2 bq[kBitsAhead];
+#pragma unroll
+        for (int i = 0; i < kBitsAhead; ++i) bq[i] = load_bits(h + 2 * i);
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = h; kb < nkb; kb += 2) {
             const int s = kb % kStages;
             const uint32_t ph = (kb / kStages) & 1;
-            const uint32_t b_nn = load_bits(kb + 2);
+            const uint2 b_cur = bq[0];
+#pragma unroll
+            for (int i = 0; i + 1 < kBitsAhead; ++i) bq[i] = bq[i + 1];
+            bq[kBitsAhead - 1] = load_bits(kb + 2 * kBitsAhead);
             const bool got = mbar_wait(&full[s], ph, a.wait_ns, abort_flag);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 if (lane == 0) give_up(abort_flag, a.status);
@@ -275,29 +306,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             uint8_t *rowp = sW + s * kWBytes + r * 128;
-            uint4 *p[kChunks];
-            uint4 w[kChunks];
+            uint4 w[8];
 #pragma unroll
-            for (int cc = 0; cc < kChunks; ++cc) {
-                p[cc] = reinterpret_cast<uint4 *>(rowp + (((kChunks * h + cc) ^ (r & 7)) << 4));
-                w[cc] = *p[cc];
-            }
+            for (int cc = 0; cc < 8; ++cc) w[cc] = *reinterpret_cast<const uint4 *>(rowp + ((cc ^ (r & 7)) << 4));
 #pragma unroll
-            for (int cc = 0; cc < kChunks; ++cc) {
-                const uint32_t byte = (b_cur >> (8 * cc)) & 0xFFu;
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint32_t byte = ((cc < 4 ? b_cur.x : b_cur.y) >> (8 * (cc & 3))) & 0xFFu;
                 w[cc].x = rebuild_pair<0>(w[cc].x, byte, neg_al);
                 w[cc].y = rebuild_pair<1>(w[cc].y, byte, neg_al);
                 w[cc].z = rebuild_pair<2>(w[cc].z, byte, neg_al);
                 w[cc].w = rebuild_pair<3>(w[cc].w, byte, neg_al);
-                if constexpr (!kTmemA) *p[cc] = w[cc];
+                if constexpr (!kTmemA) *reinterpret_cast<uint4 *>(rowp + ((cc ^ (r & 7)) << 4)) = w[cc];
             }
             if constexpr (kTmemA) {
-                static_assert(kChunks == 4, "one 16-column TMEM store per thread and K block");
-                const uint32_t v[16] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w,
-                                        w[2].x, w[2].y, w[2].z, w[2].w, w[3].x, w[3].y, w[3].z, w[3].w};
-                tmem_st_32x32b_x16(tmem + (static_cast<uint32_t>(sub * 32) << 16) + kAccCols + s * (kBK / 2) +
-                                       16 * h,
-                                   v);
+                uint32_t v[32];
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    v[4 * cc] = w[cc].x, v[4 * cc + 1] = w[cc].y;
+                    v[4 * cc + 2] = w[cc].z, v[4 * cc + 3] = w[cc].w;
+                }
+                tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(sub * 32) << 16) + kAccCols + s * (kBK / 2), v);
                 tmem_st_wait();
                 tc_fence_before();
             } else {
@@ -305,11 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&rebuilt[s]);
-            b_cur = b_nxt;
-            b_nxt = b_nn;
         }
-
-        if (ok) {
+        if (ok && !kGrouped && a.ksplit > 1) {
+            // Split K: park this rank's fp32 partial tile in the (now idle) ring
+            // memory as red[token][row]; the cluster adds the ranks' tiles below.
+            const bool got = mbar_wait(acc_full, 0, a.wait_ns, abort_flag);
+            if (__all_sync(0xFFFFFFFFu, got)) {
+                tc_fence_after();
+                const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+                float *red = reinterpret_cast<float *>(smem);
+#pragma unroll 1
+                for (int c0 = h * (kBN / kParts); c0 < (h + 1) * (kBN / kParts); c0 += 32) {
+                    if (c0 >= count) break;  // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(lane_addr + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) red[(c0 + i) * kBM + r] = __uint_as_float(v[i]);
+                }
+            } else if (lane == 0) {
+                give_up(abort_flag, a.status);
+            }
+        } else if (ok) {
             const bool got = mbar_wait(acc_full, 0, a.wait_ns, abort_flag);
             if (__all_sync(0xFFFFFFFFu, got)) {
                 tc_fence_after();
@@ -343,18 +388,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+
+    if (!kGrouped && a.ksplit > 1) {
+        // rank c adds elements [c*share, (c+1)*share) of the tile over the cluster's
+        // ranks in rank order and writes them as bf16 (consecutive threads: consecutive rows)
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int rank = static_cast<int>(cluster.block_rank());
+        const int total = count * kBM;
+        const int share = (total + a.ksplit - 1) / a.ksplit;
+        const int e1 = min(total, (rank + 1) * share);
+        float *red = reinterpret_cast<float *>(smem);
+        if (!*abort_flag) {
+            for (int e = rank * share + threadIdx.x; e < e1; e += kThreads) {
+                const int tok = e / kBM, rr = e - tok * kBM;
+                const int64_t orow = static_cast<int64_t>(m0) + rr;
+                if (orow < a.n_out) {
+                    float sum = 0.0f;
+                    for (int q = 0; q < a.ksplit; ++q) sum += cluster.map_shared_rank(red, q)[e];
+                    __nv_bfloat16 hv = __float2bfloat16_rn(sum);
+                    a.y[(static_cast<int64_t>(n0) + tok) * a.n_out + orow] = *reinterpret_cast<uint16_t *>(&hv);
+                }
+            }
+        }
+        cluster.sync();  // peers may still be reading this CTA's tile
+    }
 }
 
 }  // namespace
 
 namespace {
 
-template <bool kGrouped, bool kTmemA>
+template <bool kGrouped, bool kTmemA, int BN>
 cudaError_t set_smem_attr(const DevCtx &ctx) {
     static bool attr_set[128] = {false};
     if (ctx.device < 128 && !attr_set[ctx.device]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kGrouped, kTmemA>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kGrouped, kTmemA, BN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(Tile<BN>::kSmemBytes));
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
@@ -385,11 +456,62 @@ void fill_common(PrefillArgs &a, int64_t m, int64_t n_out, int64_t n_in, void *y
 }
 
 bool make_maps(CUtensorMap &tm_w, CUtensorMap &tm_x, const void *w_base, const void *x, int64_t x_rows,
-               int64_t n_out, int64_t n_in) {
+               int64_t n_out, int64_t n_in, int bn) {
     return encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kBK, kBM,
                                 CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, x_rows, n_in * 2, kBK, kBN,
-                                CU_TENSOR_MAP_SWIZZLE_128B);
+           encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, x_rows, n_in * 2, kBK,
+                                static_cast<uint32_t>(bn), CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace
+
+namespace {
+
+template <int BN>
+cudaError_t launch_prefill_bn(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                              int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                              cudaStream_t stream) {
+    const bool tmem_a = use_tmem_a();
+    cudaError_t e = tmem_a ? set_smem_attr<false, true, BN>(ctx) : set_smem_attr<false, false, BN>(ctx);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm_w, tm_x;
+    if (!make_maps(tm_w, tm_x, w_base, x, m, n_out, n_in, BN)) return cudaErrorInvalidValue;
+    PrefillArgs a = {};
+    fill_common(a, m, n_out, n_in, y, ctx);
+    a.bits = bits;
+    a.alpha = alpha;
+    a.mode = alpha_mode;
+    a.tok_tiles = static_cast<int32_t>((m + BN - 1) / BN);
+    a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
+    a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
+    const int64_t tiles = static_cast<int64_t>(a.row_tiles) * a.tok_tiles;
+    // Few output tiles (small m, or few W rows) leave SMs idle: split K over a
+    // cluster of C CTAs (one CTA per SM; a cluster sits in one GPC, so at most
+    // ~90% of the SMs are counted on), each rank keeping at least 8 K blocks.
+    int c = 1;
+    while (c < 8 && tiles * (2 * c) * 10 <= 9 * static_cast<int64_t>(ctx.num_sms) && a.num_kb / (2 * c) >= 8) c *= 2;
+    if (const char *ev = std::getenv("BD_PREFILL_KSPLIT")) {
+        const int f = std::atoi(ev);
+        if (f == 1 || f == 2 || f == 4 || f == 8) c = f;
+    }
+    a.kb_per = (a.num_kb + c - 1) / c;
+    a.ksplit = (a.num_kb + a.kb_per - 1) / a.kb_per;  // no empty ranks
+    const int64_t grid = tiles * a.ksplit;
+    if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Tile<BN>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.ksplit);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return tmem_a ? cudaLaunchKernelEx(&cfg, prefill_kernel<false, true, BN>, tm_w, tm_x, a)
+                  : cudaLaunchKernelEx(&cfg, prefill_kernel<false, false, BN>, tm_w, tm_x, a);
 }
 
 }  // namespace
@@ -397,36 +519,19 @@ bool make_maps(CUtensorMap &tm_w, CUtensorMap &tm_x, const void *w_base, const v
 cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                            int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                            cudaStream_t stream) {
-    const bool tmem_a = use_tmem_a();
-    cudaError_t e = tmem_a ? set_smem_attr<false, true>(ctx) : set_smem_attr<false, false>(ctx);
-    if (e != cudaSuccess) return e;
-    CUtensorMap tm_w, tm_x;
-    if (!make_maps(tm_w, tm_x, w_base, x, m, n_out, n_in)) return cudaErrorInvalidValue;
-    PrefillArgs a = {};
-    fill_common(a, m, n_out, n_in, y, ctx);
-    a.bits = bits;
-    a.alpha = alpha;
-    a.mode = alpha_mode;
-    a.tok_tiles = static_cast<int32_t>((m + kBN - 1) / kBN);
-    a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
-    a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
-    const int64_t tiles = static_cast<int64_t>(a.row_tiles) * a.tok_tiles;
-    if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    if (tmem_a)
-        prefill_kernel<false, true><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
-    else
-        prefill_kernel<false, false><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
-    return cudaGetLastError();
+    if (m <= 64)
+        return launch_prefill_bn<64>(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
+    return launch_prefill_bn<256>(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
 }
 
 cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
                                    int64_t n_out, int64_t n_in, void *y, const GroupTable &tab, const DevCtx &ctx,
                                    cudaStream_t stream) {
     const bool tmem_a = use_tmem_a();
-    cudaError_t e = tmem_a ? set_smem_attr<true, true>(ctx) : set_smem_attr<true, false>(ctx);
+    cudaError_t e = tmem_a ? set_smem_attr<true, true, 256>(ctx) : set_smem_attr<true, false, 256>(ctx);
     if (e != cudaSuccess) return e;
     CUtensorMap tm_w, tm_x;
-    if (!make_maps(tm_w, tm_x, w_base, x_sorted, m, n_out, n_in)) return cudaErrorInvalidValue;
+    if (!make_maps(tm_w, tm_x, w_base, x_sorted, m, n_out, n_in, 256)) return cudaErrorInvalidValue;
     PrefillArgs a = {};
     fill_common(a, m, n_out, n_in, y, ctx);
     bool vec8 = (n_in / 8) % 8 == 0;
@@ -441,12 +546,16 @@ cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *
     a.n_tiles = tab.n_tiles;
     a.perm = tab.perm;
     a.max_slots = tab.max_slots;
+    a.ksplit = 1;
+    a.kb_per = a.num_kb;
     const int64_t grid = static_cast<int64_t>(a.row_tiles) * tab.max_slots;
     if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     if (tmem_a)
-        prefill_kernel<true, true><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+        prefill_kernel<true, true, 256><<<static_cast<unsigned>(grid), kThreads, Tile<256>::kSmemBytes, stream>>>(
+            tm_w, tm_x, a);
     else
-        prefill_kernel<true, false><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(tm_w, tm_x, a);
+        prefill_kernel<true, false, 256><<<static_cast<unsigned>(grid), kThreads, Tile<256>::kSmemBytes, stream>>>(
+            tm_w, tm_x, a);
     return cudaGetLastError();
 }
 

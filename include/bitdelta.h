@@ -134,9 +134,10 @@ int32_t bd_compress_noalloc(const void *w_base, const void *w_ft,
  *
  *   y[t, j] = sum_k x[t, k] * (W_base[j, k] + alpha_(j) * s_jk),
  *   s_jk = +1 if bit(j, k) else -1, alpha_(j) = alpha[0] or alpha[j].
- * Accumulation is fp32; y is rounded once to bf16.  Small m streams W_base
- * and the bits from HBM once; large m runs a tensor-core (tcgen05) kernel
- * that rebuilds each W tile in shared memory as bf16(W_base + alpha*s).
+ * Accumulation is fp32; y is rounded once to bf16.  m <= 16 streams W_base
+ * and the bits from HBM once (mma.sync, distributive form); larger m runs a
+ * tensor-core (tcgen05) kernel that rebuilds each W tile on chip as
+ * bf16(W_base + alpha*s), splitting K over a cluster when its tiles are few.
  *
  *   x       bf16 [m, n_in]      (read; m may be 0, then nothing is launched)
  *   w_base  bf16 [n_out, n_in]  (read)
@@ -228,9 +229,9 @@ int32_t bd_get_device_status(void *stream);
 int64_t bd_set_wait_limit_ns(int64_t limit_ns);
 
 /* Debug knob: which fused-linear kernel later bd_linear calls use.
- * 0 = automatic (the HBM-streaming kernel for m <= 64 when its activation
- * slice fits in shared memory, the tensor-core kernel otherwise); 1 = always
- * the streaming kernel (BD_ERR_UNSUPPORTED_SHAPE where it cannot run);
+ * 0 = automatic (the HBM-streaming kernel for m <= 16 when it can run, the
+ * tensor-core kernel otherwise); 1 = always the streaming kernel (m <= 64;
+ * BD_ERR_UNSUPPORTED_SHAPE where it cannot run);
  * 2 = always the tensor-core kernel; 3 = always the register-fed streaming
  * kernel (the fallback of 1 for n_in not a multiple of 128).  Other values
  * are ignored.  Returns the previous value. */
