@@ -611,7 +611,8 @@ def run_kernel_case(args):
 
     --kernel-case linear:N_OUTxN_IN:M[:path], compress:N_OUTxN_IN[:mode],
                   grouped:N_OUTxN_IN:M:V (V variants, uniform ids), reconstruct:N_OUTxN_IN
-                  (W_eff materialised) or reconstruct_mm:N_OUTxN_IN:M (W_eff + a cuBLAS matmul)
+                  (W_eff materialised), reconstruct_mm:N_OUTxN_IN:M (W_eff + a cuBLAS matmul) or
+                  cache_load:N_OUTxN_IN (a delta's cold load through the delta cache)
     Rotates over enough copies of the weights that the working set exceeds L2.
     """
     from bit_delta_tenant_gb300 import build as lib_build
@@ -624,7 +625,8 @@ def run_kernel_case(args):
     n_out, n_in = (int(v) for v in shape.split("x"))
     per = 2.0 * n_out * n_in
     copies = max(1, int(np.ceil(3 * 129e6 / per)))
-    mats = [synth.matrix_pair(n_out, n_in, 0.02, 1e-3, 50 + i, dev) for i in range(copies)]
+    mats = [synth.matrix_pair(n_out, n_in, 0.02, 1e-3, 50 + i, dev) for i in range(copies)] \
+        if kind != "cache_load" else []
     if kind == "linear":
         m = int(parts[2])
         path = int(parts[3]) if len(parts) > 3 else 0
@@ -671,6 +673,39 @@ def run_kernel_case(args):
         # reconstruct alone: its own traffic; with the matmul: the fused linear's algorithmic bytes
         work = decode_bytes(m, n_out, n_in, 0) if m else 4.0 * n_out * n_in + n_out * n_in / 8
         flops = 2.0 * m * n_out * n_in
+    elif kind == "cache_load":
+        # cold start of a variant through the delta cache: two variants alternate in
+        # an arena that holds one, so every request loads its delta from pinned host memory
+        bpm = n_out * n_in // 8
+        hosts = [(torch.randint(0, 256, (bpm,), dtype=torch.uint8).pin_memory(),
+                  torch.full((n_out,), 1e-3, dtype=torch.float32).pin_memory()) for _ in range(2)]
+        block = (bpm + 255) // 256 * 256 + (4 * n_out + 255) // 256 * 256
+        arena = torch.empty(block + 256, dtype=torch.uint8, device=dev)
+        cache = bd.DeltaCache(2, arena, half_life_s=1.0)
+        for v, (hb, ha) in enumerate(hosts):
+            cache.register(v, hb, ha)
+        stream = torch.cuda.Stream()
+        for i in range(args.warmup + 1):
+            rc, _, _ = cache.acquire(i % 2, stream=stream)
+            cache.release(i % 2, stream=stream)
+        torch.cuda.synchronize()
+        reps = max(args.steps, 4)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(reps):
+            rc, _, _ = cache.acquire(i % 2, stream=stream)
+            assert rc == bd.BD_OK
+            cache.release(i % 2, stream=stream)
+        t1.record(stream)
+        t1.synchronize()
+        sec = t0.elapsed_time(t1) * 1e-3 / reps
+        nbytes = bpm + 4 * n_out
+        st = cache.stats()
+        cache.close()
+        print(json.dumps({"kernel_case": args.kernel_case, "load_us": sec * 1e6, "h2d_GB/s": nbytes / sec / 1e9,
+                          "loads": st.loads, "evictions": st.evictions,
+                          "cold_start_70b_variant_ms": 70e9 / 8 / (nbytes / sec) * 1e3}), flush=True)
+        return
     elif kind == "grouped":
         m, nv = int(parts[2]), int(parts[3])
         bd.bd_set_weight_prefetch(0)

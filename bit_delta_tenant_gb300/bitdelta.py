@@ -25,6 +25,7 @@ BD_ERR_WORKSPACE = 4
 BD_ERR_CUDA = 5
 BD_ERR_DEVICE_TIMEOUT = 6
 BD_ERR_BAD_VARIANT_ID = 7
+BD_ERR_NO_SPACE = 8
 BD_ALPHA_SCALAR = 0
 BD_ALPHA_PER_ROW = 1
 BD_MAX_VARIANTS = 64
@@ -61,6 +62,24 @@ def load_library(path: str | None = None):
         lib.bd_set_linear_path.restype = I32
         lib.bd_reconstruct.argtypes = [V, V, V, I32, I64, I64, V, V]
         lib.bd_reconstruct.restype = I32
+        lib.bd_cache_state_size.argtypes = [I32]
+        lib.bd_cache_state_size.restype = SZ
+        lib.bd_cache_create.argtypes = [V, SZ, I32, V, SZ, ctypes.c_double, I32, ctypes.POINTER(V)]
+        lib.bd_cache_create.restype = I32
+        lib.bd_cache_destroy.argtypes = [V]
+        lib.bd_cache_destroy.restype = I32
+        lib.bd_cache_register.argtypes = [V, I32, V, SZ, V, SZ]
+        lib.bd_cache_register.restype = I32
+        lib.bd_cache_set_pinned.argtypes = [V, I32, I32]
+        lib.bd_cache_set_pinned.restype = I32
+        lib.bd_cache_acquire.argtypes = [V, I32, ctypes.c_double, V, ctypes.POINTER(V), ctypes.POINTER(V)]
+        lib.bd_cache_acquire.restype = I32
+        lib.bd_cache_release.argtypes = [V, I32, V]
+        lib.bd_cache_release.restype = I32
+        lib.bd_cache_get_stats.argtypes = [V, ctypes.POINTER(CacheStats)]
+        lib.bd_cache_get_stats.restype = I32
+        lib.bd_cache_is_resident.argtypes = [V, I32]
+        lib.bd_cache_is_resident.restype = I32
         lib.bd_set_weight_prefetch.argtypes = [I32]
         lib.bd_set_weight_prefetch.restype = I32
         lib.bd_get_device_status.argtypes = [V]
@@ -113,6 +132,75 @@ def bd_set_wait_limit_ns(limit_ns: int) -> int:
 
 def bd_set_linear_path(path: int) -> int:
     return int(load_library().bd_set_linear_path(int(path)))
+
+
+class CacheStats(ctypes.Structure):
+    _fields_ = [("acquires", ctypes.c_int64), ("hits", ctypes.c_int64), ("misses", ctypes.c_int64),
+                ("joined", ctypes.c_int64), ("loads", ctypes.c_int64), ("evictions", ctypes.c_int64),
+                ("bytes_loaded", ctypes.c_int64), ("resident_bytes", ctypes.c_int64),
+                ("resident", ctypes.c_int32), ("in_use", ctypes.c_int32)]
+
+
+class DeltaCache:
+    """Thin owner of a bd_cache: the state buffer (host), the arena (a torch
+    tensor on the device, or a host tensor with host_arena=True) and the host
+    deltas it registers are kept alive here; every call is the C entry point."""
+
+    def __init__(self, max_variants: int, arena: torch.Tensor, half_life_s: float = 10.0, host_arena: bool = False):
+        lib = load_library()
+        size = lib.bd_cache_state_size(int(max_variants))
+        if size == 0:
+            raise ValueError("max_variants out of range")
+        self._state = ctypes.create_string_buffer(size)
+        self._arena = arena
+        self._keep = {}
+        self._handle = ctypes.c_void_p()
+        self._host = bool(host_arena)
+        rc = lib.bd_cache_create(ctypes.addressof(self._state), size, int(max_variants), _ptr(arena),
+                                 arena.numel() * arena.element_size(), float(half_life_s), 1 if host_arena else 0,
+                                 ctypes.byref(self._handle))
+        _check(rc, "bd_cache_create")
+
+    def register(self, variant: int, bits: torch.Tensor, alpha: torch.Tensor) -> None:
+        rc = load_library().bd_cache_register(self._handle, int(variant), _ptr(bits), bits.numel(), _ptr(alpha),
+                                              alpha.numel() * 4)
+        _check(rc, "bd_cache_register")
+        self._keep[variant] = (bits, alpha)
+
+    def set_pinned(self, variant: int, pinned: bool) -> None:
+        _check(load_library().bd_cache_set_pinned(self._handle, int(variant), 1 if pinned else 0), "bd_cache_set_pinned")
+
+    def acquire(self, variant: int, now_s: float = -1.0, stream=None):
+        """(status, bits_ptr, alpha_ptr) -- raw device (or arena) addresses."""
+        b, a = ctypes.c_void_p(), ctypes.c_void_p()
+        rc = load_library().bd_cache_acquire(self._handle, int(variant), float(now_s), self._s(stream),
+                                             ctypes.byref(b), ctypes.byref(a))
+        return int(rc), b.value or 0, a.value or 0
+
+    def release(self, variant: int, stream=None) -> int:
+        return int(load_library().bd_cache_release(self._handle, int(variant), self._s(stream)))
+
+    def _s(self, stream):
+        return ctypes.c_void_p(0) if self._host else _stream(stream)
+
+    def stats(self) -> CacheStats:
+        st = CacheStats()
+        _check(load_library().bd_cache_get_stats(self._handle, ctypes.byref(st)), "bd_cache_get_stats")
+        return st
+
+    def is_resident(self, variant: int) -> bool:
+        return bool(load_library().bd_cache_is_resident(self._handle, int(variant)))
+
+    def close(self) -> None:
+        if self._handle:
+            _check(load_library().bd_cache_destroy(self._handle), "bd_cache_destroy")
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def bd_set_weight_prefetch(enable: int) -> int:

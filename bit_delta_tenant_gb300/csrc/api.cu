@@ -129,6 +129,7 @@ BD_API const char *bd_status_string(int32_t status) {
         case BD_ERR_CUDA: return "CUDA runtime error";
         case BD_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
         case BD_ERR_BAD_VARIANT_ID: return "variant id outside [0, n_variants)";
+        case BD_ERR_NO_SPACE: return "delta cache: no evictable delta leaves room for the request";
         default: return "unknown status";
     }
 }

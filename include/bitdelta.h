@@ -27,7 +27,8 @@
  *   - Every pointer is a DEVICE pointer unless marked "host".  The caller
  *     allocates and owns every buffer (inputs, outputs and workspace); the
  *     library allocates nothing, frees nothing and keeps no pointer after a
- *     call returns.
+ *     call returns -- except the delta cache (bd_cache_*), which keeps its
+ *     caller-provided state, arena and host deltas until bd_cache_destroy.
  *   - Every device pointer must be 16-byte aligned; n_in must be a multiple of
  *     8 (one packed byte per 8 inputs).  Any n_in that is a multiple of 8, any
  *     n_out >= 1 and any m >= 0 are handled on the GPU (ragged tails included).
@@ -58,7 +59,8 @@ typedef enum bd_status {
     BD_ERR_WORKSPACE = 4,         /* workspace missing or smaller than required */
     BD_ERR_CUDA = 5,              /* a CUDA runtime call failed                 */
     BD_ERR_DEVICE_TIMEOUT = 6,    /* a bounded device-side wait ran out         */
-    BD_ERR_BAD_VARIANT_ID = 7     /* a variant id outside [0, n_variants)       */
+    BD_ERR_BAD_VARIANT_ID = 7,    /* a variant id outside [0, n_variants)       */
+    BD_ERR_NO_SPACE = 8           /* delta cache: nothing evictable leaves room  */
 } bd_status;
 
 /* How alpha is stored ([math]: one per matrix; [infra]: one per output row). */
@@ -208,6 +210,73 @@ int32_t bd_linear_grouped(const void *x, const int32_t *variant_ids, int64_t m,
                           const int32_t *alpha_modes_v, int32_t n_variants,
                           int64_t n_out, int64_t n_in, void *y, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Delta cache  ([infra] "Détails d'infrastructure": each variant's delta is
+ * loaded from host memory into HBM on its first request -- the cold start --
+ * resident deltas are evicted least-recently-used weighted by request rate,
+ * popular ones can be pinned, and concurrent requests for one variant share a
+ * single load; [serve] the base stays resident, a request names its variant)
+ *
+ * The one stateful part of the library.  The caller provides a host buffer of
+ * bd_cache_state_size(max_variants) bytes for the state and a 256-byte
+ * aligned device arena that the cache carves first-fit into
+ * 256-byte aligned blocks (freed blocks coalesce); the cache keeps pointers to
+ * both, and to the registered host deltas, until bd_cache_destroy.  In CUDA
+ * mode it creates 9 CUDA events per registered variant (destroyed by
+ * bd_cache_destroy); register the host deltas from pinned memory for
+ * asynchronous copies.
+ *
+ * Eviction rule (the page only names it): every variant keeps a request rate
+ * that gains 1 per acquire and halves every `half_life_s` seconds; the victim
+ * is the resident variant that is not pinned and not acquired, with the lowest
+ * decayed rate, the least recently requested one on ties.  Variants are
+ * evicted until the new block fits; BD_ERR_NO_SPACE if none is left.
+ *
+ * Ordering: a load is cudaMemcpyAsync of the bits, then of alpha, on the
+ * acquiring stream, followed by an event; an acquirer that finds the load
+ * still queued makes its stream wait on that event (single flight, counted in
+ * `joined`).  bd_cache_release records an event on the given stream; before
+ * an evicted variant's block is reused the host waits for its outstanding
+ * releases (and its load), so no copy overwrites a delta that queued work
+ * still reads.  host_arena != 0: the arena is host memory, loads are memcpy
+ * and no CUDA call is made (policy studies, CPU tests).  All calls are
+ * thread-safe (one mutex per cache).
+ *
+ * `now_s` (acquire) is the request time in seconds for the rate; pass a
+ * negative value to use the library's monotonic clock.
+ * Errors: BD_ERR_INVALID_ARG, BD_ERR_WORKSPACE (state buffer too small),
+ *         BD_ERR_MISALIGNED (arena), BD_ERR_BAD_VARIANT_ID (id outside
+ *         [0, max_variants) or not registered), BD_ERR_NO_SPACE, BD_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+#define BD_CACHE_MAX_VARIANTS 4096
+
+typedef struct bd_cache bd_cache;
+
+typedef struct bd_cache_stats {
+    int64_t acquires, hits, misses, joined, loads, evictions, bytes_loaded;
+    int64_t resident_bytes;
+    int32_t resident, in_use;
+} bd_cache_stats;
+
+size_t  bd_cache_state_size(int32_t max_variants);
+int32_t bd_cache_create(void *state_host, size_t state_bytes, int32_t max_variants,
+                        void *arena, size_t arena_bytes, double half_life_s,
+                        int32_t host_arena, bd_cache **out);
+int32_t bd_cache_destroy(bd_cache *cache);
+/* host_bits [bits_bytes] and host_alpha [alpha_bytes] stay owned by the caller
+ * and must outlive the cache. */
+int32_t bd_cache_register(bd_cache *cache, int32_t variant, const void *host_bits, size_t bits_bytes,
+                          const float *host_alpha, size_t alpha_bytes);
+int32_t bd_cache_set_pinned(bd_cache *cache, int32_t variant, int32_t pinned);
+/* Device pointers of the variant's bits and alpha (256-byte aligned), valid
+ * until the matching bd_cache_release; loads the delta on a miss. */
+int32_t bd_cache_acquire(bd_cache *cache, int32_t variant, double now_s, void *stream,
+                         const uint8_t **bits, const float **alpha);
+int32_t bd_cache_release(bd_cache *cache, int32_t variant, void *stream);
+int32_t bd_cache_get_stats(bd_cache *cache, bd_cache_stats *out);
+/* 1 if the variant's delta is in the arena, else 0. */
+int32_t bd_cache_is_resident(bd_cache *cache, int32_t variant);
 
 /* ------------------------------------------------------------------------ *
  * Status and debugging
