@@ -58,6 +58,11 @@ cudaError_t launch_decode(const void *x, int64_t m, const void *w_base, const ui
                           int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                           cudaStream_t stream);
 
+// y32 = x . W_base^T in fp32 ([m, n_out] row-major) on the tensor-core kernel, W_base taken as
+// stored (the shared base product of the multi-tenant path).
+cudaError_t launch_base_product(const void *x, int64_t m, const void *w_base, int64_t n_out, int64_t n_in,
+                                float *y32, const DevCtx &ctx, cudaStream_t stream);
+
 // W_eff = bf16(fp32(W_base) + alpha * s) materialised in HBM (for a standard matmul).
 cudaError_t launch_reconstruct(const void *w_base, const uint8_t *bits, const float *alpha, int32_t alpha_mode,
                                int64_t n_out, int64_t n_in, void *w_eff, const DevCtx &ctx, cudaStream_t stream);
@@ -110,7 +115,7 @@ bool grouped_decode_supported(int64_t m, int32_t n_variants, int64_t n_in, const
 cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
                                   int64_t n_out, int64_t n_in, void *y, const int32_t *s_tiles,
                                   const int32_t *n_s_tiles, const int32_t *perm, const int32_t *n_valid,
-                                  const DevCtx &ctx, cudaStream_t stream);
+                                  const float *ybase, const DevCtx &ctx, cudaStream_t stream);
 
 size_t grouped_workspace_size(int64_t m, int32_t n_variants, int64_t n_out, int64_t n_in);
 cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const void *w_base,

@@ -16,10 +16,10 @@
 //      BD_ERR_BAD_VARIANT_ID in the status word and their tokens are skipped.
 //   2. gather: the activations in variant order (a plain row copy).
 //   3. compute: small batches (m <= 64) run a streaming kernel that reads
-//      W_base and every variant's bits once (grouped_decode.cu on mma.sync; a
-//      tcgen05 variant, grouped_decode_tc.cu, is selectable); larger ones the
-//      tensor-core kernel over per-variant token tiles (prefill.cu).  Outputs go straight back to
-//      the original token rows.
+//      W_base and every variant's bits once (grouped_decode.cu on mma.sync;
+//      a tcgen05 variant and a base-on-tensor-cores split are selectable);
+//      larger batches the tensor-core kernel over per-variant token tiles
+//      (prefill.cu).  Outputs go straight back to the original token rows.
 #include <cstdlib>
 
 #include "bd_device.cuh"
@@ -37,11 +37,11 @@ constexpr int kMaxSignTilesRead = 24;  // the streaming kernel reads this many t
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct WsLayout {
-    size_t seg, perm, tiles, n_tiles, s_tiles, n_s_tiles, xs, total;
+    size_t seg, perm, tiles, n_tiles, s_tiles, n_s_tiles, xs, ybase, total;
     int64_t max_slots, max_s_tiles;
 };
 
-WsLayout layout(int64_t m, int32_t nv, int64_t n_in) {
+WsLayout layout(int64_t m, int32_t nv, int64_t n_out, int64_t n_in) {
     WsLayout L;
     L.max_slots = (m + kTileRows - 1) / kTileRows + nv;
     L.max_s_tiles = (m + kPad - 1) / kPad + nv + kMaxSignTilesRead;  // room for the streaming kernel's fixed read
@@ -60,6 +60,9 @@ WsLayout layout(int64_t m, int32_t nv, int64_t n_in) {
     off = align256(off + sizeof(int32_t));
     L.xs = off;
     off = align256(off + 2 * static_cast<size_t>(m > 0 ? m : 1) * static_cast<size_t>(n_in));
+    // fp32 base product of the split small-batch path (only for m <= 64)
+    L.ybase = off;
+    if (m <= 64) off = align256(off + 4 * static_cast<size_t>(m > 0 ? m : 1) * static_cast<size_t>(n_out));
     L.total = off;
     return L;
 }
@@ -185,14 +188,13 @@ __global__ void group_gather_kernel(const uint4 *x, int64_t vec_per_row, const i
 }  // namespace
 
 size_t grouped_workspace_size(int64_t m, int32_t n_variants, int64_t n_out, int64_t n_in) {
-    (void)n_out;
-    return layout(m, n_variants, n_in).total;
+    return layout(m, n_variants, n_out, n_in).total;
 }
 
 cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const void *w_base,
                            const GroupedVariants &vars, int64_t n_out, int64_t n_in, void *y, void *ws,
                            size_t ws_bytes, const DevCtx &ctx, cudaStream_t stream) {
-    const WsLayout L = layout(m, vars.count, n_in);
+    const WsLayout L = layout(m, vars.count, n_out, n_in);
     if (ws_bytes < L.total) return cudaErrorInvalidValue;
     uint8_t *base = static_cast<uint8_t *>(ws);
     SortArgs s;
@@ -222,18 +224,30 @@ cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const v
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    // Small batches: the mma.sync streaming kernel (fastest measured on GB300:
-    // the tcgen05 streaming kernel issues ~4 N=16 MMAs per variant and K block,
-    // each with an mbarrier round trip, and ends up latency-bound).
-    // BD_GROUPED_PATH=1/2/3 forces tcgen05 streaming / mma.sync streaming /
-    // per-variant tiles (tests and comparisons; unsupported shapes fall through).
+    // Small batches (default): the mma.sync streaming kernel computing the base
+    // and every variant's sign products in one pass.  BD_GROUPED_PATH=1/2/3/4
+    // forces the tcgen05 streaming kernel / that default / per-variant
+    // tensor-core tiles / a split in which the tensor-core kernel computes the
+    // base product (fp32, W_base as stored) and the streaming kernel only the
+    // sign products (tests and comparisons; unsupported shapes fall through).
+    // Measured on GB300 (14 variants, 64 tokens): the split matches the single
+    // kernel (195 us for 8192 x 8192), the sign products dominate; the tcgen05
+    // streaming kernel issues ~4 N=16 MMAs per variant and K block, each
+    // behind an mbarrier round trip, and ends up latency-bound.
     const char *force = std::getenv("BD_GROUPED_PATH");
     const int path = force ? std::atoi(force) : 0;
     if (path == 1 && grouped_decode_tc_supported(m, vars.count, n_in, xs, w_base, vars))
         return launch_grouped_decode_tc(xs, m, w_base, vars, n_out, n_in, y, s.seg, s.perm, ctx, stream);
-    if ((path == 0 || path == 1 || path == 2) && grouped_decode_supported(m, vars.count, n_in, w_base, vars))
+    if (path == 4 && m <= 64 && grouped_decode_supported(m, vars.count, n_in, w_base, vars)) {
+        float *ybase = reinterpret_cast<float *>(base + L.ybase);
+        e = launch_base_product(xs, m, w_base, n_out, n_in, ybase, ctx, stream);
+        if (e != cudaSuccess) return e;
         return launch_grouped_decode(xs, m, w_base, vars, n_out, n_in, y, s.s_tiles, s.n_s_tiles, s.perm,
-                                     s.seg + vars.count, ctx, stream);
+                                     s.seg + vars.count, ybase, ctx, stream);
+    }
+    if ((path == 0 || path == 1 || path == 2 || path == 4) && grouped_decode_supported(m, vars.count, n_in, w_base, vars))
+        return launch_grouped_decode(xs, m, w_base, vars, n_out, n_in, y, s.s_tiles, s.n_s_tiles, s.perm,
+                                     s.seg + vars.count, nullptr, ctx, stream);
     GroupTable tab;
     tab.tiles = s.tiles;
     tab.n_tiles = s.n_tiles;

@@ -43,11 +43,14 @@ constexpr int kMaxS = 24;  // sign tiles of 8 tokens: m/8 + (variants present) <
 constexpr uint32_t kBoxBytes = 64 * 64 * 2;
 constexpr uint32_t kBitsBox = kRows * 16;
 
-template <int NTB>
+// SIGN = true: the sign products only (the shared base product comes from the
+// tensor-core kernel as fp32 and is added in the epilogue), so stages carry no W.
+template <int NTB, bool SIGN>
 struct GdRing {
     static constexpr uint32_t kXBox = NTB * 1024;  // 8*NTB token rows x 128 bytes
-    static constexpr uint32_t kStageBytes = 2 * kBoxBytes + 2 * kXBox + kMaxVar * kBitsBox;
-    static constexpr int kStages = NTB >= 4 ? 4 : 5;
+    static constexpr uint32_t kWBytes = SIGN ? 0 : 2 * kBoxBytes;
+    static constexpr uint32_t kStageBytes = kWBytes + 2 * kXBox + kMaxVar * kBitsBox;
+    static constexpr int kStages = SIGN ? 6 : NTB >= 4 ? 4 : 5;
     static constexpr uint32_t kRedBytes = 8 * NTB * kRows * 4;
     static constexpr uint32_t kTableBytes = kMaxVar * kRows * 4 + 3 * kMaxS * 4 + 16;
     static constexpr size_t kSmem = 1024 + kStages * kStageBytes + kRedBytes + kTableBytes + 2 * kStages * 8 + 16;
@@ -68,6 +71,7 @@ struct GdArgs {
     const int32_t *perm;       // sorted row -> original token
     const int32_t *n_valid;    // tokens with a valid id
     uint16_t *y;
+    const float *ybase;        // sign-only kernel: x . W_base^T in fp32, [sorted row][n_out]
     int64_t m, n_out, n_in, ks;
     int32_t cluster;
     unsigned *status;
@@ -97,10 +101,10 @@ __device__ __forceinline__ void signs8(const uint8_t *p, const uint32_t (&mul)[4
     }
 }
 
-template <int NTB>
+template <int NTB, bool SIGN>
 __global__ void __launch_bounds__(kThreads, 1)
     gdecode_kernel(const __grid_constant__ GdMaps maps, const __grid_constant__ GdArgs a) {
-    using R = GdRing<NTB>;
+    using R = GdRing<NTB, SIGN>;
     constexpr int MP = 8 * NTB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,17 +175,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slot j % kStages once all warps released that slot's previous step.  A
     // warp blocks only for the step it is about to consume; otherwise it
     // refills between its own steps without waiting.
-    const int n_boxes = 4 + a.nv;
-    auto box_bytes = [&](int bx) -> uint32_t { return bx < 2 ? kBoxBytes : bx < 4 ? R::kXBox : kBitsBox; };
+    constexpr int nW = SIGN ? 0 : 2;  // W boxes first (none for the sign-only kernel), then x, then bits
+    const int n_boxes = nW + 2 + a.nv;
+    auto box_bytes = [&](int bx) -> uint32_t { return bx < nW ? kBoxBytes : bx < nW + 2 ? R::kXBox : kBitsBox; };
     const uint32_t my_tx = (warp < n_boxes ? box_bytes(warp) : 0u) + (warp + 16 < n_boxes ? box_bytes(warp + 16) : 0u);
     int issued = 0;
     auto issue_box = [&](int bx, int kc, uint8_t *st, uint64_t *bar) {
-        if (bx < 2)
+        if (bx < nW)
             tma_load_2d(st + bx * kBoxBytes, &maps.w, bar, kc + 64 * bx, row0);
-        else if (bx < 4)
-            tma_load_2d(st + 2 * kBoxBytes + (bx - 2) * R::kXBox, &maps.x, bar, kc + 64 * (bx - 2), 0);
+        else if (bx < nW + 2)
+            tma_load_2d(st + R::kWBytes + (bx - nW) * R::kXBox, &maps.x, bar, kc + 64 * (bx - nW), 0);
         else
-            tma_load_2d(st + 2 * kBoxBytes + 2 * R::kXBox + (bx - 4) * kBitsBox, &maps.b[bx - 4], bar, kc / 8, row0);
+            tma_load_2d(st + R::kWBytes + 2 * R::kXBox + (bx - nW - 2) * kBitsBox, &maps.b[bx - nW - 2], bar, kc / 8,
+                        row0);
     };
     auto issue = [&](int j) {  // lane 0 only
         const int s = j % R::kStages;
@@ -193,10 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (lane == 0) {
         if (warp == 0) {
-            tma_prefetch_desc(&maps.w);
+            if (!SIGN) tma_prefetch_desc(&maps.w);
             tma_prefetch_desc(&maps.x);
         }
-        if (warp >= 4 && warp < n_boxes) tma_prefetch_desc(&maps.b[warp - 4]);
+        if (warp >= nW + 2 && warp < n_boxes) tma_prefetch_desc(&maps.b[warp - nW - 2]);
         for (; issued < n_steps && issued < R::kStages; ++issued) issue(issued);
     }
     {
@@ -244,13 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *st = smem + s * R::kStageBytes;
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
+            const uint8_t *xbox = st + R::kWBytes + kh * R::kXBox;
+            const uint8_t *bits = st + R::kWBytes + 2 * R::kXBox + kh * 8;
+            if constexpr (!SIGN) {
             const uint8_t *box = st + kh * kBoxBytes;
             const uint4 wa0 = lds128(box + r0 * 128 + sw0), wa1 = lds128(box + r0 * 128 + sw1);
             const uint4 wb0 = lds128(box + (r0 + 8) * 128 + sw0), wb1 = lds128(box + (r0 + 8) * 128 + sw1);
             const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
             const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
-            const uint8_t *xbox = st + 2 * kBoxBytes + kh * R::kXBox;
-            const uint8_t *bits = st + 2 * kBoxBytes + 2 * R::kXBox + kh * 8;
             // base: this warp's 8-token tiles of all tokens (sorted order)
 #pragma unroll
             for (int ib = 0; ib < NB; ++ib) {
@@ -264,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_bf16_16816(accb[ib], wa[2 * j], wb[2 * j], wa[2 * j + 1], wb[2 * j + 1], xv[2 * j],
                                        xv[2 * j + 1]);
                 }
+            }
             }
             // signs: this warp's tiles in interleaved pairs (a missing second tile is empty)
 #pragma unroll
@@ -306,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     (void)ok;
 
-    // ---- red[sorted token][row] = base + alpha * signs (each token in one base and one sign tile) ----
+    // ---- red[sorted token][row] = base + alpha * signs (each token in one base and one sign tile;
+    //      the sign-only kernel adds its base in the cluster sum below) ----
+    if constexpr (!SIGN) {
 #pragma unroll
     for (int ib = 0; ib < NB; ++ib) {
         const int tt = 4 * ib + tq;
@@ -314,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float *p = red + (8 * tt + 2 * t) * kRows + r0;
             p[0] = accb[ib][0], p[kRows] = accb[ib][1], p[8] = accb[ib][2], p[kRows + 8] = accb[ib][3];
         }
+    }
     }
     __syncthreads();
 #pragma unroll
@@ -324,13 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float al0 = alpha_s[v * kRows + r0], al1 = alpha_s[v * kRows + r0 + 8];
             if (2 * t < cnt) {
                 float *p = red + (start + 2 * t) * kRows + r0;
-                p[0] += al0 * accs[i][0];
-                p[8] += al1 * accs[i][2];
+                p[0] = (SIGN ? 0.0f : p[0]) + al0 * accs[i][0];
+                p[8] = (SIGN ? 0.0f : p[8]) + al1 * accs[i][2];
             }
             if (2 * t + 1 < cnt) {
                 float *p = red + (start + 2 * t + 1) * kRows + r0;
-                p[0] += al0 * accs[i][1];
-                p[8] += al1 * accs[i][3];
+                p[0] = (SIGN ? 0.0f : p[0]) + al0 * accs[i][1];
+                p[8] = (SIGN ? 0.0f : p[8]) + al1 * accs[i][3];
             }
         }
     }
@@ -345,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lr = rank * share + (i - tok * share);
         const int64_t row = static_cast<int64_t>(row0) + lr;
         if (lr < kRows && row < a.n_out) {
-            float s = 0.0f;
+            float s = SIGN ? a.ybase[static_cast<int64_t>(tok) * a.n_out + row] : 0.0f;
             for (int q = 0; q < a.cluster; ++q) s += cluster.map_shared_rank(red, q)[tok * kRows + lr];
             __nv_bfloat16 h = __float2bfloat16_rn(s);
             a.y[static_cast<int64_t>(a.perm[tok]) * a.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
@@ -354,20 +365,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster.sync();
 }
 
-template <int NTB>
+template <int NTB, bool SIGN>
 cudaError_t launch_ntb(const GdMaps &maps, const GdArgs &a, int64_t row_blocks, const DevCtx &ctx,
                        cudaStream_t stream) {
     static bool attr_set[128] = {false};
     if (ctx.device < 128 && !attr_set[ctx.device]) {
-        cudaError_t e = cudaFuncSetAttribute(gdecode_kernel<NTB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(GdRing<NTB>::kSmem));
+        cudaError_t e = cudaFuncSetAttribute(gdecode_kernel<NTB, SIGN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(GdRing<NTB, SIGN>::kSmem));
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(row_blocks * a.cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = GdRing<NTB>::kSmem;
+    cfg.dynamicSmemBytes = GdRing<NTB, SIGN>::kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -378,7 +389,18 @@ cudaError_t launch_ntb(const GdMaps &maps, const GdArgs &a, int64_t row_blocks, 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gdecode_kernel<NTB>, maps, a);
+    return cudaLaunchKernelEx(&cfg, gdecode_kernel<NTB, SIGN>, maps, a);
+}
+
+template <bool SIGN>
+cudaError_t launch_sel(int ntb, const GdMaps &maps, const GdArgs &a, int64_t row_blocks, const DevCtx &ctx,
+                       cudaStream_t stream) {
+    switch (ntb) {
+        case 1: return launch_ntb<1, SIGN>(maps, a, row_blocks, ctx, stream);
+        case 2: return launch_ntb<2, SIGN>(maps, a, row_blocks, ctx, stream);
+        case 4: return launch_ntb<4, SIGN>(maps, a, row_blocks, ctx, stream);
+        default: return launch_ntb<8, SIGN>(maps, a, row_blocks, ctx, stream);
+    }
 }
 
 }  // namespace
@@ -396,7 +418,7 @@ bool grouped_decode_supported(int64_t m, int32_t n_variants, int64_t n_in, const
 cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
                                   int64_t n_out, int64_t n_in, void *y, const int32_t *s_tiles,
                                   const int32_t *n_s_tiles, const int32_t *perm, const int32_t *n_valid,
-                                  const DevCtx &ctx, cudaStream_t stream) {
+                                  const float *ybase, const DevCtx &ctx, cudaStream_t stream) {
     const int ntb = m <= 8 ? 1 : m <= 16 ? 2 : m <= 32 ? 4 : 8;
     GdMaps maps;
     if (!encode_tensor_map_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, 64, kRows,
@@ -419,6 +441,7 @@ cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w
     a.perm = perm;
     a.n_valid = n_valid;
     a.y = static_cast<uint16_t *>(y);
+    a.ybase = ybase;
     a.m = m;
     a.n_out = n_out;
     a.n_in = n_in;
@@ -435,12 +458,8 @@ cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w
     a.ks = per * kStepK;
     a.cluster = static_cast<int32_t>((steps + per - 1) / per);
     if (row_blocks * a.cluster > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    switch (ntb) {
-        case 1: return launch_ntb<1>(maps, a, row_blocks, ctx, stream);
-        case 2: return launch_ntb<2>(maps, a, row_blocks, ctx, stream);
-        case 4: return launch_ntb<4>(maps, a, row_blocks, ctx, stream);
-        default: return launch_ntb<8>(maps, a, row_blocks, ctx, stream);
-    }
+    return ybase != nullptr ? launch_sel<true>(ntb, maps, a, row_blocks, ctx, stream)
+                            : launch_sel<false>(ntb, maps, a, row_blocks, ctx, stream);
 }
 
 }  // namespace bd

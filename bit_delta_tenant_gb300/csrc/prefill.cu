@@ -70,6 +70,7 @@ struct PrefillArgs {
     const uint8_t *bits;
     const float *alpha;
     uint16_t *y;
+    float *y32;         // base-only mode (non-null): y32 = x . W_base^T in fp32, no rebuild, A read as loaded
     int64_t m, n_out, n_in;
     int32_t mode;
     int32_t num_kb;
@@ -263,15 +264,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = sub * 32 + lane;
         const int64_t row = static_cast<int64_t>(m0) + r;
         const bool row_ok = row < a.n_out;
-        const float al = row_ok ? (mode ? alpha[row] : alpha[0]) : 0.0f;
+        const float al = (row_ok && alpha != nullptr) ? (mode ? alpha[row] : alpha[0]) : 0.0f;  // none: base only
         const uint32_t neg_al = __float_as_uint(-al);
         const int64_t bpr = a.n_in / 8;
-        const uint8_t *brow = bits + (row_ok ? row : 0) * bpr;
+        const uint8_t *brow = bits != nullptr ? bits + (row_ok ? row : 0) * bpr : nullptr;
 
         auto load_bits = [&](int kbl) -> uint2 {  // kbl: this CTA's K block index
             uint2 v = make_uint2(0u, 0u);
             const int64_t c0 = static_cast<int64_t>(kb0 + kbl) * 8;  // first packed byte
-            if (row_ok && kbl < nkb) {
+            if (row_ok && kbl < nkb && a.y32 == nullptr) {
                 if (a.bits_vec8 && c0 + 8 <= bpr) {
                     v = __ldg(reinterpret_cast<const uint2 *>(brow + c0));
                 } else {
@@ -304,6 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) give_up(abort_flag, a.status);
                 ok = false;
                 break;
+            }
+            if (!kTmemA && a.y32 != nullptr) {  // base only: the MMA takes the W_base tile as loaded
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rebuilt[s]);
+                continue;
             }
             uint8_t *rowp = sW + s * kWBytes + r * 128;
             uint4 w[8];
@@ -372,8 +378,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c0 + i < count) {
                                 const int64_t t = kGrouped ? static_cast<int64_t>(a.perm[n0 + c0 + i])
                                                            : static_cast<int64_t>(n0) + c0 + i;
-                                __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[i]));
-                                ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&hv);
+                                if (!kGrouped && a.y32 != nullptr) {
+                                    a.y32[t * a.n_out + row] = __uint_as_float(v[i]);
+                                } else {
+                                    __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[i]));
+                                    ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&hv);
+                                }
                             }
                         }
                     }
@@ -406,8 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (orow < a.n_out) {
                     float sum = 0.0f;
                     for (int q = 0; q < a.ksplit; ++q) sum += cluster.map_shared_rank(red, q)[e];
-                    __nv_bfloat16 hv = __float2bfloat16_rn(sum);
-                    a.y[(static_cast<int64_t>(n0) + tok) * a.n_out + orow] = *reinterpret_cast<uint16_t *>(&hv);
+                    if (a.y32 != nullptr) {
+                        a.y32[(static_cast<int64_t>(n0) + tok) * a.n_out + orow] = sum;
+                    } else {
+                        __nv_bfloat16 hv = __float2bfloat16_rn(sum);
+                        a.y[(static_cast<int64_t>(n0) + tok) * a.n_out + orow] = *reinterpret_cast<uint16_t *>(&hv);
+                    }
                 }
             }
         }
@@ -470,8 +484,8 @@ namespace {
 template <int BN>
 cudaError_t launch_prefill_bn(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                               int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
-                              cudaStream_t stream) {
-    const bool tmem_a = use_tmem_a();
+                              cudaStream_t stream, float *y32 = nullptr) {
+    const bool tmem_a = y32 == nullptr && use_tmem_a();  // base-only reads A from shared memory
     cudaError_t e = tmem_a ? set_smem_attr<false, true, BN>(ctx) : set_smem_attr<false, false, BN>(ctx);
     if (e != cudaSuccess) return e;
     CUtensorMap tm_w, tm_x;
@@ -481,6 +495,7 @@ cudaError_t launch_prefill_bn(const void *x, int64_t m, const void *w_base, cons
     a.bits = bits;
     a.alpha = alpha;
     a.mode = alpha_mode;
+    a.y32 = y32;
     a.tok_tiles = static_cast<int32_t>((m + BN - 1) / BN);
     a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
     a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
@@ -522,6 +537,13 @@ cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const u
     if (m <= 64)
         return launch_prefill_bn<64>(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
     return launch_prefill_bn<256>(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
+}
+
+cudaError_t launch_base_product(const void *x, int64_t m, const void *w_base, int64_t n_out, int64_t n_in,
+                                float *y32, const DevCtx &ctx, cudaStream_t stream) {
+    if (m <= 64)
+        return launch_prefill_bn<64>(x, m, w_base, nullptr, nullptr, 0, n_out, n_in, nullptr, ctx, stream, y32);
+    return launch_prefill_bn<256>(x, m, w_base, nullptr, nullptr, 0, n_out, n_in, nullptr, ctx, stream, y32);
 }
 
 cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,

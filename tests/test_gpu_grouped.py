@@ -143,7 +143,8 @@ def test_fourteen_variant_workload_full_size(kind, grouped_path):
     assert_y_close(yh[ts, js], y_ref, mag, f"14-variant {kind}")
 
 
-@pytest.fixture(params=["1", "2", "3"], ids=["tcgen05_stream", "mma_stream", "per_variant_tiles"])
+@pytest.fixture(params=["1", "2", "3", "4"], ids=["tcgen05_stream", "mma_stream", "per_variant_tiles",
+                                                  "base_tc_signs_mma"])
 def grouped_path(request, monkeypatch):
     """Force one multi-tenant kernel (shapes a kernel cannot take fall through to the next)."""
     monkeypatch.setenv("BD_GROUPED_PATH", request.param)
