@@ -368,6 +368,80 @@ class GroupedWorkload(Workload):
         return run, f"first {frac_rows:.4g} of the rows: 14 compressions + the multi-tenant linear"
 
 
+class GroupedStackWorkload(Workload):
+    """The serving decode step over a whole model: every linear of the 32-layer
+    Llama-3-8B-shape stack as one multi-tenant call, 64 tokens whose ids are
+    uniform over 14 variants, all 224 calls replayed as one CUDA graph.
+
+    The 14 variants' deltas are resident (as behind the delta cache); their sign
+    bits are seeded random bytes (a Laplace delta's signs are balanced) and their
+    alpha the variant's scale, so no fine-tuned weights have to be held (14 x 14 GB);
+    the compression of the stack is measured by the llama3_8b_stack_* workloads."""
+
+    def __init__(self, bd, dev):
+        c = workloads.LLAMA3_8B_STACK
+        g14 = workloads.GROUPED_14
+        self.cfg = c
+        self.metric_unit = "GB/s"
+        nv, m = g14["n_variants"], g14["decode_m"]
+        scales = workloads.variant_scales(g14)
+        ids = synth.uniform_ids(m, nv, g14["seed"])
+        self.ids_h = ids
+        self.ids = torch.from_numpy(ids).to(dev)
+        active = len(set(ids.tolist()))
+        shapes = [(n, k) for _ in range(c["layers"]) for (_, n, k) in c["matrices"]]
+        self.xs, self.ys, self.wss = {}, {}, {}
+        calls, nbytes, flops = [], 0.0, 0.0
+        self.first = None
+        for i, (n_out, n_in) in enumerate(shapes):
+            gen = synth.generator(workloads.matrix_seed(c["seed"], 1000 + i), dev)
+            wb = synth.bf16_normal((n_out, n_in), c["sigma"], gen, dev)
+            bits_v = [torch.randint(0, 256, (n_out, n_in // 8), generator=gen, device=dev, dtype=torch.uint8)
+                      for _ in range(nv)]
+            alpha_v = [torch.full((1,), float(b), dtype=torch.float32, device=dev) for b in scales]
+            if n_in not in self.xs:
+                self.xs[n_in] = synth.activations(m, n_in, 20_000 + n_in, dev)
+                self.wss[n_in] = {}
+            if n_out not in self.ys:
+                self.ys[n_out] = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+            key = (n_out, n_in)
+            if key not in self.wss[n_in]:
+                self.wss[n_in][key] = torch.empty((bd.bd_linear_grouped_workspace_size(m, nv, n_out, n_in),),
+                                                  dtype=torch.uint8, device=dev)
+            x, y, ws = self.xs[n_in], self.ys[n_out], self.wss[n_in][key]
+            calls.append(lambda x=x, wb=wb, bv=bits_v, av=alpha_v, y=y, ws=ws:
+                         bd.bd_linear_grouped(x, self.ids, wb, bv, av, [0] * nv, y, ws))
+            nbytes += 2.0 * n_out * n_in + active * n_out * n_in / 8 + 4.0 * nv + 2.0 * m * n_in + 2.0 * m * n_out
+            flops += 2.0 * m * n_out * n_in
+            if self.first is None:
+                self.first = (wb, bits_v, alpha_v, x)
+        self.lin = Phase("grouped_linear", calls, bytes_=nbytes, flops=flops, launches=3 * len(calls), bound="hbm")
+        self.phases = [self.lin]
+        self.dominant = self.lin
+        self.h2d_tensors = list(self.xs.values()) + [self.ids]
+        self.d2h_tensors = list(self.ys.values())
+        self.config = {"workload": "llama3_8b_stack_grouped14_decode", "layers": c["layers"],
+                       "matrices": sorted({f"{a}x{b}" for _, a, b in c["matrices"]}), "variants": nv, "tokens": m,
+                       "ids": "uniform", "active_variants": active,
+                       "deltas": "resident; seeded random sign bits, alpha = the variant's Laplace scale",
+                       "l2": "inputs larger than L2 (14 GB of base weights and 12 GB of bits per step)"}
+
+    def oracle_sample(self, oracle, frac_rows: float):
+        wb, bits_v, alpha_v, x = self.first
+        n = max(8, int(wb.shape[0] * frac_rows))
+        wbh = synth.as_u16(wb[:n])
+        bh = [b[:n].cpu().numpy() for b in bits_v]
+        ah = [a.cpu().numpy() for a in alpha_v]
+        xh = synth.as_u16(x)
+        modes = np.zeros(len(bh), np.int32)
+
+        def run():
+            oracle.linear_grouped(xh, self.ids_h, wbh, bh, ah, modes)
+            mm = xh.shape[0]
+            return 2.0 * wbh.size + len(bh) * wbh.size / 8 + 2.0 * mm * wbh.shape[1] + 2.0 * mm * n
+        return run, f"first {frac_rows:.4g} of the rows of the first matrix: the multi-tenant linear"
+
+
 WORKLOADS = {
     "llama7b_layer_decode": lambda bd, dev: LayerWorkload(
         bd, dev, workloads.LLAMA7B_LAYER, workloads.LLAMA7B_LAYER["ms"], "GB/s", "llama7b_layer_decode"),
@@ -379,6 +453,7 @@ WORKLOADS = {
     "llama3_8b_stack_decode": lambda bd, dev: LayerWorkload(
         bd, dev, workloads.LLAMA3_8B_STACK, (1,), "GB/s", "llama3_8b_stack_decode",
         layers=workloads.LLAMA3_8B_STACK["layers"], private_io=False),
+    "llama3_8b_stack_grouped14_decode": lambda bd, dev: GroupedStackWorkload(bd, dev),
     "llama3_8b_stack_prefill": lambda bd, dev: LayerWorkload(
         bd, dev, workloads.LLAMA3_8B_STACK, (2048,), "TFLOP/s", "llama3_8b_stack_prefill",
         layers=workloads.LLAMA3_8B_STACK["layers"], private_io=False),
