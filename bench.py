@@ -132,9 +132,16 @@ def max_over_ranks(ws, value: float) -> float:
     if ws == 1:
         return value
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_value(ws: int, steps: int, step_work: float, t_max_ms: float) -> float:
+    """Whole-job throughput of N replicas (weak scaling): every rank processes
+    `steps` steps of `step_work` units; the slowest rank's time counts."""
+    return ws * steps * step_work / (t_max_ms * 1e-3) / 1e9
 
 
 # --------------------------------------------------------------------------- workloads
@@ -515,7 +522,7 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status after timing: {bd.bd_status_string(status)}")
 
     t_max = max_over_ranks(ws, total_ms)
-    value = ws * args.steps * wl.step_work() / (t_max * 1e-3) / 1e9
+    value = aggregate_value(ws, args.steps, wl.step_work(), t_max)
 
     dom = wl.dominant
     dom_idx = wl.phases.index(dom)
