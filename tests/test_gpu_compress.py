@@ -62,9 +62,19 @@ def test_hand_worked_bytes_on_gpu(case):
     assert np.array_equal(bits.cpu().numpy(), expect)
 
 
+@pytest.fixture(params=["direct", "ring"])
+def compress_form(request, monkeypatch):
+    """Both forms of pass 1 (the default direct one, and the persistent ring one)."""
+    if request.param == "ring":
+        monkeypatch.setenv("BD_COMPRESS_RING", "1")
+    else:
+        monkeypatch.delenv("BD_COMPRESS_RING", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("n_out,n_in", [(1, 8), (7, 24), (33, 120), (129, 136), (128, 4096), (3, 16392)])
 @pytest.mark.parametrize("mode", [0, 1])
-def test_ragged_shapes(n_out, n_in, mode):
+def test_ragged_shapes(n_out, n_in, mode, compress_form):
     w_base, w_ft = synth.matrix_pair(n_out, n_in, 0.02, 1e-3, seed=n_out * 31 + n_in, device="cuda")
     check_against_oracle(w_base, w_ft, mode)
 
@@ -97,6 +107,18 @@ def test_llama70b_matrices_per_row_alpha(idx):
 def test_alpha_is_bitwise_reproducible(mode):
     w_base, w_ft = synth.matrix_pair(4096, 11008, 0.02, 1e-3, seed=5, device="cuda")
     b1, a1 = gpu_compress(w_base, w_ft, mode)
+    b2, a2 = gpu_compress(w_base, w_ft, mode)
+    assert torch.equal(b1, b2)
+    assert torch.equal(a1.view(torch.int32), a2.view(torch.int32))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_direct_and_ring_forms_agree_bitwise(mode, monkeypatch):
+    """The two forms of pass 1 take the same summation tree, so their alpha agree to the bit."""
+    w_base, w_ft = synth.matrix_pair(2048, 11008, 0.02, 1e-3, seed=8, device="cuda")
+    monkeypatch.delenv("BD_COMPRESS_RING", raising=False)
+    b1, a1 = gpu_compress(w_base, w_ft, mode)
+    monkeypatch.setenv("BD_COMPRESS_RING", "1")
     b2, a2 = gpu_compress(w_base, w_ft, mode)
     assert torch.equal(b1, b2)
     assert torch.equal(a1.view(torch.int32), a2.view(torch.int32))
