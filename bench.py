@@ -201,6 +201,27 @@ def compress_phase(bd, mats, mode, dev):
 # since there a linear follows the compression that writes its bits.
 WEIGHT_PREFETCH = True
 
+# How a layer's fused linears are issued: "layer" passes the projections that share
+# their input in a real layer -- q, k, v and gate, up -- to one bd_linear_batch call
+# each (o and down alone, through the same entry); "none" calls bd_linear per matrix.
+LINEAR_BATCH = "layer"
+FUSED_GROUPS = ({"q", "k", "v"}, {"gate", "up"})
+
+
+def layer_groups(names):
+    """Consecutive indices of `names` ("L<l>.<matrix>") that one batched call takes."""
+    groups, i = [], 0
+    while i < len(names):
+        layer, base = names[i].split(".", 1)
+        grp = next((g for g in FUSED_GROUPS if base in g), None)
+        j = i + 1
+        while grp is not None and j < len(names) and names[j].split(".", 1)[0] == layer \
+                and names[j].split(".", 1)[1] in grp:
+            j += 1
+        groups.append(list(range(i, j)))
+        i = j
+    return groups
+
 
 def decode_bytes(m, n_out, n_in, mode):
     return 2.0 * n_out * n_in + n_out * n_in / 8 + 4.0 * (n_out if mode == 1 else 1) + 2.0 * m * n_in + 2.0 * m * n_out
@@ -244,23 +265,40 @@ class LayerWorkload(Workload):
                      for i, (_, n_out, n_in) in enumerate(shapes)]
         self.comp, self.packed = compress_phase(bd, self.mats, mode, dev)
         self.xs, self.ys = {}, {}
-        calls, nbytes, flops = [], 0.0, 0.0
+        calls, nbytes, flops, launches = [], 0.0, 0.0, 0
+        groups = layer_groups([n for n, _, _ in shapes]) if LINEAR_BATCH == "layer" else \
+            [[i] for i in range(len(shapes))]
+        self.batch_ws = None
         for m in ms:
-            for i, (_, n_out, n_in) in enumerate(shapes):
-                xk = (m, i) if private_io else (m, n_in)
-                yk = (m, i) if private_io else (m, n_out)
-                if xk not in self.xs:
-                    self.xs[xk] = synth.activations(m, n_in, 10_000 + 97 * len(self.xs) + m, dev)
-                if yk not in self.ys:
-                    self.ys[yk] = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
-                x, y = self.xs[xk], self.ys[yk]
-                wb = self.mats[i][0]
-                bits, alpha = self.packed[i]
-                calls.append(lambda x=x, wb=wb, bits=bits, alpha=alpha, y=y: bd.bd_linear(x, wb, bits, alpha, mode, y))
-                nbytes += decode_bytes(m, n_out, n_in, mode)
-                flops += 2.0 * m * n_out * n_in
+            for grp in groups:
+                probs = []
+                for i in grp:
+                    _, n_out, n_in = shapes[i]
+                    xk = (m, i) if private_io else (m, n_in)
+                    yk = (m, i) if private_io else (m, n_out)
+                    if xk not in self.xs:
+                        self.xs[xk] = synth.activations(m, n_in, 10_000 + 97 * len(self.xs) + m, dev)
+                    if yk not in self.ys:
+                        self.ys[yk] = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+                    bits, alpha = self.packed[i]
+                    probs.append((self.xs[xk], self.mats[i][0], bits, alpha, mode, self.ys[yk]))
+                    nbytes += decode_bytes(m, n_out, n_in, mode)
+                    flops += 2.0 * m * n_out * n_in
+                if LINEAR_BATCH == "layer":
+                    descs = bd.linear_descs(probs)
+                    need = bd.bd_linear_batch_workspace_size(descs)
+                    if need > 0 and (self.batch_ws is None or self.batch_ws.numel() < need):
+                        self.batch_ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+                    calls.append(lambda descs=descs: bd.bd_linear_batch(descs, self.batch_ws))
+                    batched = m <= 16 and all(p[1].shape[1] % 128 == 0 for p in probs)
+                    launches += 1 if batched else len(probs)
+                else:
+                    x, wb, bits, alpha, _, y = probs[0]
+                    calls.append(lambda x=x, wb=wb, bits=bits, alpha=alpha, y=y:
+                                 bd.bd_linear(x, wb, bits, alpha, mode, y))
+                    launches += 1
         bound = "hbm" if unit == "GB/s" else "tensor"
-        self.lin = Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=len(calls), bound=bound,
+        self.lin = Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=launches, bound=bound,
                          weight_prefetch=WEIGHT_PREFETCH)
         self.phases = [self.comp, self.lin]
         self.dominant = self.lin
@@ -269,7 +307,7 @@ class LayerWorkload(Workload):
         self.config = {"workload": name, "matrices": sorted({f"{a}x{b}" for _, a, b in shapes}),
                        "matrix_count": len(shapes), "tokens": list(ms),
                        "alpha": "per-row" if mode == 1 else "scalar", "dtype_in": "bf16 weights/activations",
-                       "weight_prefetch": WEIGHT_PREFETCH,
+                       "weight_prefetch": WEIGHT_PREFETCH, "linear_batch": LINEAR_BATCH,
                        "l2": "inputs larger than L2 (consecutive uses of a matrix separated by >250 MB of traffic)"}
 
     def oracle_sample(self, oracle, frac_rows: float):
@@ -570,19 +608,22 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-KERNEL_SOURCES = {"hbm": "decode_tma.cu", "tensor": "prefill.cu"}
+KERNEL_SOURCES = {"hbm": ("decode_tma.cu", "decode_batch.cu", "decode_stage.cuh"), "tensor": ("prefill.cu",)}
 
 
 def lookup_traffic(workload: str, phase):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
-    profiles/traffic_<workload>.md, if the kernel source is unchanged since the capture."""
+    """DRAM bytes per launch of the dominant phase's kernels from the committed ncu summary
+    profiles/traffic_<workload>.md, if their sources are unchanged since the capture (SHA-1
+    over the sources of KERNEL_SOURCES, in that order)."""
     import hashlib
     import re
     path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
-    src = os.path.join(ROOT, "bit_delta_tenant_gb300", "csrc", KERNEL_SOURCES[phase.bound])
     try:
         text = open(path).read()
-        digest = hashlib.sha1(open(src, "rb").read()).hexdigest()
+        h = hashlib.sha1()
+        for name in KERNEL_SOURCES[phase.bound]:
+            h.update(open(os.path.join(ROOT, "bit_delta_tenant_gb300", "csrc", name), "rb").read())
+        digest = h.hexdigest()
     except OSError:
         return None
     m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)\s+source_sha1:\s*([0-9a-f]+)", text)
@@ -704,6 +745,7 @@ def run_kernel_case(args):
     """One kernel on one shape, launched eagerly (no graph): for ncu captures and sweeps.
 
     --kernel-case linear:N_OUTxN_IN:M[:path], compress:N_OUTxN_IN[:mode],
+                  batch:N_OUTxN_IN:M:COUNT (COUNT linears per bd_linear_batch call),
                   grouped:N_OUTxN_IN:M:V (V variants, uniform ids), reconstruct:N_OUTxN_IN
                   (W_eff materialised), reconstruct_mm:N_OUTxN_IN:M (W_eff + a cuBLAS matmul) or
                   cache_load:N_OUTxN_IN (a delta's cold load through the delta cache)
@@ -718,7 +760,8 @@ def run_kernel_case(args):
     kind, shape = parts[0], parts[1]
     n_out, n_in = (int(v) for v in shape.split("x"))
     per = 2.0 * n_out * n_in
-    copies = max(1, int(np.ceil(3 * 129e6 / per)))
+    count = int(parts[3]) if kind == "batch" else 1  # linears per batched call
+    copies = max(1, int(np.ceil(3 * 129e6 / (per * count)))) * count
     mats = [synth.matrix_pair(n_out, n_in, 0.02, 1e-3, 50 + i, dev) for i in range(copies)] \
         if kind != "cache_load" else []
     if kind == "linear":
@@ -743,6 +786,31 @@ def run_kernel_case(args):
             bd.bd_linear(x, mats[i][0], packed[i][0], packed[i][1], 0, y)
         work = decode_bytes(m, n_out, n_in, 0)
         flops = 2.0 * m * n_out * n_in
+    elif kind == "batch":
+        # COUNT linears of one shape per bd_linear_batch call (q/k/v-like); call i takes copies
+        # i*COUNT .. i*COUNT+COUNT-1, so the copies rotate as for linear:...
+        m = int(parts[2])
+        packed = []
+        for wb, wf in mats:
+            bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=dev)
+            alpha = torch.empty((1,), dtype=torch.float32, device=dev)
+            ws = torch.empty((max(16, bd.bd_compress_workspace_size(n_out, n_in, 0)),), dtype=torch.uint8,
+                             device=dev)
+            bd.bd_compress(wb, wf, 0, bits, alpha, ws)
+            packed.append((bits, alpha))
+        x = synth.activations(m, n_in, 7, dev)
+        ys = [torch.empty((m, n_out), dtype=torch.bfloat16, device=dev) for _ in range(count)]
+        descs = [bd.linear_descs([(x, mats[c * count + j][0], packed[c * count + j][0], packed[c * count + j][1], 0,
+                                   ys[j]) for j in range(count)]) for c in range(copies // count)]
+        bws = torch.zeros(max(1, bd.bd_linear_batch_workspace_size(descs[0])), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        bd.bd_set_weight_prefetch(1 if WEIGHT_PREFETCH else 0)
+        copies //= count
+
+        def call(i):
+            bd.bd_linear_batch(descs[i], bws)
+        work = count * decode_bytes(m, n_out, n_in, 0)
+        flops = count * 2.0 * m * n_out * n_in
     elif kind in ("reconstruct", "reconstruct_mm"):
         # the page's "standard matmul in decode" reading: rebuild W_eff in HBM (and,
         # for reconstruct_mm, multiply with a cuBLAS GEMM); compare with linear:...
@@ -876,11 +944,14 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--weight-prefetch", type=int, choices=[0, 1], default=1,
                     help="capture the device-resident fused linears with bd_set_weight_prefetch(1)")
+    ap.add_argument("--linear-batch", choices=["none", "layer"], default="layer",
+                    help="layer: q/k/v and gate/up of a layer in one bd_linear_batch call each")
     ap.add_argument("--kernel-case", default=None,
                     help="linear:N_OUTxN_IN:M[:path] or compress:N_OUTxN_IN[:mode] (one kernel, eager)")
     args = ap.parse_args()
-    global WEIGHT_PREFETCH
+    global WEIGHT_PREFETCH, LINEAR_BATCH
     WEIGHT_PREFETCH = bool(args.weight_prefetch)
+    LINEAR_BATCH = args.linear_batch
     if args.kernel_case:
         run_kernel_case(args)
         return

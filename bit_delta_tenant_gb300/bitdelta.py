@@ -30,9 +30,19 @@ BD_ALPHA_SCALAR = 0
 BD_ALPHA_PER_ROW = 1
 BD_MAX_VARIANTS = 64
 BD_NOALLOC_MAX_PARTIALS = 131072
+BD_LINEAR_BATCH_MAX = 256
+BD_LINEAR_BATCH_PER_LAUNCH = 8
 
 _lock = threading.Lock()
 _lib = None
+
+
+class LinearDesc(ctypes.Structure):
+    """bd_linear_desc: one problem of bd_linear_batch (device pointers and sizes)."""
+    _fields_ = [("x", ctypes.c_void_p), ("w_base", ctypes.c_void_p), ("bits", ctypes.c_void_p),
+                ("alpha", ctypes.c_void_p), ("y", ctypes.c_void_p), ("m", ctypes.c_int64),
+                ("n_out", ctypes.c_int64), ("n_in", ctypes.c_int64), ("alpha_mode", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class BitDeltaError(RuntimeError):
@@ -92,6 +102,10 @@ def load_library(path: str | None = None):
         lib.bd_compress_noalloc.restype = I32
         lib.bd_linear.argtypes = [V, I64, V, V, V, I32, I64, I64, V, V]
         lib.bd_linear.restype = I32
+        lib.bd_linear_batch_workspace_size.argtypes = [ctypes.POINTER(LinearDesc), I32]
+        lib.bd_linear_batch_workspace_size.restype = SZ
+        lib.bd_linear_batch.argtypes = [ctypes.POINTER(LinearDesc), I32, V, SZ, V]
+        lib.bd_linear_batch.restype = I32
         lib.bd_linear_grouped_workspace_size.argtypes = [I64, I32, I64, I64]
         lib.bd_linear_grouped_workspace_size.restype = SZ
         lib.bd_linear_grouped.argtypes = [V, V, I64, V, V, V, V, I32, I64, I64, V, V, SZ, V]
@@ -247,6 +261,32 @@ def bd_linear(x: torch.Tensor, w_base: torch.Tensor, bits: torch.Tensor, alpha: 
     rc = load_library().bd_linear(_ptr(x), m, _ptr(w_base), _ptr(bits), _ptr(alpha), int(alpha_mode), n_out, n_in,
                                   _ptr(y), _stream(stream))
     _check(rc, "bd_linear")
+
+
+def linear_descs(problems) -> ctypes.Array:
+    """bd_linear_desc array from (x, w_base, bits, alpha, alpha_mode, y) tuples of tensors."""
+    arr = (LinearDesc * len(problems))()
+    for d, (x, w_base, bits, alpha, alpha_mode, y) in zip(arr, problems):
+        n_out, n_in = w_base.shape
+        d.x, d.w_base, d.bits, d.alpha, d.y = (_ptr(x).value, _ptr(w_base).value, _ptr(bits).value,
+                                               _ptr(alpha).value, _ptr(y).value)
+        d.m = x.shape[0] if x.dim() == 2 else 0
+        d.n_out, d.n_in, d.alpha_mode, d.reserved = n_out, n_in, int(alpha_mode), 0
+    return arr
+
+
+def bd_linear_batch_workspace_size(descs: ctypes.Array) -> int:
+    return int(load_library().bd_linear_batch_workspace_size(descs, len(descs)))
+
+
+def bd_linear_batch(descs: ctypes.Array, workspace: torch.Tensor | None, stream=None) -> None:
+    """Each problem's y = x . (W_base + alpha * sign)^T, independent problems batched per launch.
+
+    `descs` comes from `linear_descs`; `workspace` is a zero-filled device buffer of at
+    least `bd_linear_batch_workspace_size(descs)` bytes (left ready for the next call)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().bd_linear_batch(descs, len(descs), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "bd_linear_batch")
 
 
 def bd_linear_grouped_workspace_size(m: int, n_variants: int, n_out: int, n_in: int) -> int:

@@ -3,9 +3,11 @@
 // device status word, the wait-limit knob, path dispatch for the fused
 // linear, and tensor-map encoding through the runtime's driver entry point
 // (so the library needs no link-time dependency on the driver library).
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "bd_internal.h"
 #include "bitdelta.h"
@@ -196,8 +198,10 @@ BD_API int32_t bd_compress(const void *w_base, const void *w_ft, int64_t n_out, 
 
 // ---------------------------------------------------------------- fused linear
 
-BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
-                         int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, void *stream) {
+namespace {
+
+int32_t validate_linear(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                        int32_t alpha_mode, int64_t n_out, int64_t n_in, const void *y) {
     if (m < 0) return BD_ERR_INVALID_ARG;
     if (!w_base || !bits || !alpha) return BD_ERR_INVALID_ARG;
     if (m > 0 && (!x || !y)) return BD_ERR_INVALID_ARG;
@@ -207,11 +211,12 @@ BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uin
     if (m >= BD_MAX_DIM) return BD_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(w_base) || !aligned16(bits) || !aligned16(alpha)) return BD_ERR_MISALIGNED;
     if (m > 0 && (!aligned16(x) || !aligned16(y))) return BD_ERR_MISALIGNED;
-    if (m == 0) return BD_OK;
-    bd::DevCtx ctx;
-    const int32_t rc = make_ctx(&ctx);
-    if (rc != BD_OK) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return BD_OK;
+}
+
+// One validated linear with m >= 1 on the path the knob selects.
+int32_t run_linear(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                   int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const bd::DevCtx &ctx, cudaStream_t s) {
     const int32_t path = g_linear_path.load();
     const bool tma_ok = bd::decode_tma_supported(m, n_out, n_in, w_base, bits, ctx);
     const bool decode_ok = tma_ok || bd::decode_supported(m, n_out, n_in, ctx.num_sms);
@@ -230,6 +235,114 @@ BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uin
     if (use_decode)
         return cuda_status(bd::launch_decode(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));
     return cuda_status(bd::launch_prefill(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, s));
+}
+
+// Splits a validated batch into launches of the batched streaming kernel
+// (problems grouped by m <= 8 / m <= 16, at most kBatchMaxProblems each) and
+// problems that run alone.
+struct BatchSchedule {
+    std::vector<std::vector<bd::BatchItem>> launches;
+    std::vector<int32_t> alone;
+};
+int32_t schedule_batch(const bd_linear_desc *d, int32_t n, BatchSchedule &out) {
+    if (n < 0 || n > BD_LINEAR_BATCH_MAX) return BD_ERR_INVALID_ARG;
+    if (n > 0 && d == nullptr) return BD_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i) {
+        if (d[i].reserved != 0) return BD_ERR_INVALID_ARG;
+        const int32_t rc = validate_linear(d[i].x, d[i].m, d[i].w_base, d[i].bits, d[i].alpha, d[i].alpha_mode,
+                                           d[i].n_out, d[i].n_in, d[i].y);
+        if (rc != BD_OK) return rc;
+    }
+    const int32_t path = g_linear_path.load();
+    // A launch of one linear gains nothing from the shared split: it runs as bd_linear
+    // (the cluster-split kernel) unless BD_BATCH_SINGLE=1 keeps it (measurements).
+    const char *single_env = std::getenv("BD_BATCH_SINGLE");
+    const size_t min_size = single_env != nullptr && single_env[0] == '1' ? 1 : 2;
+    std::vector<int32_t> group[2];  // problems of the batched kernel, by token tiles
+    for (int32_t i = 0; i < n; ++i) {
+        const bd_linear_desc &q = d[i];
+        if (q.m == 0) continue;
+        if ((path == 0 || path == 1) && bd::decode_batch_supported(q.m, q.n_out, q.n_in, q.x, q.w_base, q.bits, q.y))
+            group[q.m <= 8 ? 0 : 1].push_back(i);
+        else
+            out.alone.push_back(i);
+    }
+    for (const auto &g : group) {
+        for (size_t first = 0; first < g.size(); first += bd::kBatchMaxProblems) {
+            const size_t count = std::min(g.size() - first, static_cast<size_t>(bd::kBatchMaxProblems));
+            if (count < min_size) {
+                out.alone.insert(out.alone.end(), g.begin() + first, g.begin() + first + count);
+                continue;
+            }
+            std::vector<bd::BatchItem> items;
+            for (size_t k = first; k < first + count; ++k) {
+                const bd_linear_desc &q = d[g[k]];
+                items.push_back({q.x, q.w_base, q.bits, q.alpha, q.y, q.m, q.n_out, q.n_in, q.alpha_mode});
+            }
+            out.launches.push_back(items);
+        }
+    }
+    return BD_OK;
+}
+
+}  // namespace
+
+BD_API int32_t bd_linear(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                         int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, void *stream) {
+    const int32_t v = validate_linear(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y);
+    if (v != BD_OK) return v;
+    if (m == 0) return BD_OK;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    return run_linear(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, static_cast<cudaStream_t>(stream));
+}
+
+BD_API size_t bd_linear_batch_workspace_size(const bd_linear_desc *descs, int32_t n) {
+    BatchSchedule sch;
+    if (schedule_batch(descs, n, sch) != BD_OK || sch.launches.empty()) return 0;
+    bd::DevCtx ctx;
+    if (make_ctx(&ctx) != BD_OK) return 0;
+    size_t need = 0;
+    for (const auto &g : sch.launches) {
+        const bd::BatchPlan pl = bd::plan_decode_batch(g.data(), static_cast<int>(g.size()), ctx);
+        if (pl.ok && pl.workspace_bytes > need) need = pl.workspace_bytes;
+    }
+    return need;
+}
+
+BD_API int32_t bd_linear_batch(const bd_linear_desc *descs, int32_t n, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+    BatchSchedule sch;
+    const int32_t v = schedule_batch(descs, n, sch);
+    if (v != BD_OK) return v;
+    if (sch.launches.empty() && sch.alone.empty()) return BD_OK;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::vector<bd::BatchPlan> plans;
+    for (const auto &g : sch.launches) {
+        plans.push_back(bd::plan_decode_batch(g.data(), static_cast<int>(g.size()), ctx));
+        if (!plans.back().ok) return BD_ERR_CUDA;
+        if (plans.back().workspace_bytes > 0 &&
+            (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+             workspace_bytes < plans.back().workspace_bytes))
+            return BD_ERR_WORKSPACE;
+    }
+    // Launches share the workspace: each one's accesses follow the previous one's completion on the stream.
+    for (size_t i = 0; i < sch.launches.size(); ++i) {
+        const int32_t r = cuda_status(bd::launch_decode_batch(sch.launches[i].data(),
+                                                              static_cast<int>(sch.launches[i].size()), plans[i],
+                                                              workspace, ctx, s));
+        if (r != BD_OK) return r;
+    }
+    for (int32_t i : sch.alone) {
+        const bd_linear_desc &q = descs[i];
+        const int32_t r = run_linear(q.x, q.m, q.w_base, q.bits, q.alpha, q.alpha_mode, q.n_out, q.n_in, q.y, ctx, s);
+        if (r != BD_OK) return r;
+    }
+    return BD_OK;
 }
 
 BD_API int32_t bd_reconstruct(const void *w_base, const uint8_t *bits, const float *alpha, int32_t alpha_mode,

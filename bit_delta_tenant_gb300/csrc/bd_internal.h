@@ -75,6 +75,37 @@ cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, cons
                               int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                               cudaStream_t stream);
 
+// Several independent streaming linears (m <= kBatchMaxM each) in one launch
+// with the K steps of all of them split evenly over the resident CTAs
+// (decode_batch.cu).  The workspace holds one counter per 64-row block (zero
+// between launches) and the fp32 partials of blocks split between CTAs.
+constexpr int kBatchMaxProblems = 8;
+constexpr int64_t kBatchMaxM = 16;
+struct BatchItem {
+    const void *x;
+    const void *w_base;
+    const uint8_t *bits;
+    const float *alpha;
+    void *y;
+    int64_t m, n_out, n_in;
+    int32_t alpha_mode;
+};
+struct BatchPlan {
+    bool ok;
+    int nt;                 // token tiles of 8 (from the largest m)
+    int64_t grid;           // CTAs
+    int64_t total_items;    // (64-row block, 128-column K step) pairs over all linears
+    int64_t blocks;         // 64-row blocks over all linears
+    int32_t parts_max;      // most CTAs sharing one block
+    size_t counter_bytes;   // counters at the start of the workspace (256-byte multiple)
+    size_t workspace_bytes;
+};
+bool decode_batch_supported(int64_t m, int64_t n_out, int64_t n_in, const void *x, const void *w_base,
+                            const uint8_t *bits, const void *y);
+BatchPlan plan_decode_batch(const BatchItem *items, int n, const DevCtx &ctx);
+cudaError_t launch_decode_batch(const BatchItem *items, int n, const BatchPlan &plan, void *workspace,
+                                const DevCtx &ctx, cudaStream_t stream);
+
 // Tensor-core (tcgen05 + TMA) kernel for any m.
 cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                            int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,

@@ -36,37 +36,21 @@
 #include <cstdio>
 #include <cstdlib>
 
-#include "bd_device.cuh"
 #include "bd_internal.h"
+#include "decode_stage.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace bd {
 namespace {
 
-constexpr int kStepK = 128;                 // K columns per stage
+using dstage::kStepK;
+using dstage::StageLayout;
+using dstage::stage_layout;
+
 constexpr int kMaxSmem = 227 * 1024;        // opt-in dynamic shared memory per CTA on sm_103
 constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory of one SM (1 KB of it reserved per CTA)
 
-// Stage layout for R row groups (rows = 16R) and NT token tiles (MP = 8NT):
-// [W box k0..63: rows x 128 B][W box k64..127][bits: rows x 16 B, padded to
-// 1 KB][x box k0..63: MP x 128 B][x box k64..127]; every box starts on a
-// 1024-byte boundary (the 128-byte swizzle pattern repeats there).
-struct StageLayout {
-    uint32_t w_box, bits_off, bits_bytes, x_off, x_box, stage, tx;
-};
-__host__ __device__ constexpr StageLayout stage_layout(int rg, int nt) {
-    StageLayout L{};
-    const uint32_t rows = 16u * rg;
-    L.w_box = rows * 128u;
-    L.bits_off = 2u * L.w_box;
-    L.bits_bytes = rows * 16u;
-    L.x_off = L.bits_off + (L.bits_bytes + 1023u) / 1024u * 1024u;
-    L.x_box = 1024u * nt;
-    L.stage = L.x_off + 2u * L.x_box;
-    L.tx = 2u * L.w_box + L.bits_bytes + 2u * L.x_box;  // bytes the copies deliver
-    return L;
-}
 __host__ __device__ constexpr uint32_t red_bytes(int rg, int nt) { return 8u * nt * 16u * rg * 4u; }
 inline size_t smem_bytes(int rg, int nt, int stages) {
     return 1024 + static_cast<size_t>(stages) * stage_layout(rg, nt).stage + red_bytes(rg, nt) + 2 * stages * 8 + 16;
@@ -85,8 +69,6 @@ struct TmaDecodeArgs {
     unsigned *status;
     uint64_t wait_ns;
 };
-
-__device__ __forceinline__ uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
 
 __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *status) {
     *abort_flag = 1;
@@ -197,8 +179,7 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     } else {
         // ---- consumers ----
         // Token rows of the x boxes use the same swizzle term as W rows: (8*tt + g) & 7 == r0 & 7 == g.
-        const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ (r0 & 7)) << 4);
-        const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ (r0 & 7)) << 4);  // rows r0, r0+8 share r&7
+        const dstage::LaneSwizzle sw = dstage::lane_swizzle(t, r0);
         int s = 0;
         uint32_t ph = 0;
         for (int i = 0; i < n_steps; ++i, (++s == kStages ? (s = 0, ph ^= 1u) : 0u)) {
@@ -207,45 +188,7 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
                 if (lane == 0) give_up(abort_flag, a.status);
                 break;
             }
-            const uint8_t *st = smem + s * L.stage;
-            const uint8_t *box = st + kh * L.w_box;
-            const uint4 wa0 = lds128(box + r0 * 128 + sw0);
-            const uint4 wa1 = lds128(box + r0 * 128 + sw1);
-            const uint4 wb0 = lds128(box + (r0 + 8) * 128 + sw0);
-            const uint4 wb1 = lds128(box + (r0 + 8) * 128 + sw1);
-            const uint8_t *bt = st + L.bits_off;
-            const uint32_t ba = *reinterpret_cast<const uint16_t *>(bt + r0 * 16 + kh * 8 + 2 * t);
-            const uint32_t bb = *reinterpret_cast<const uint16_t *>(bt + (r0 + 8) * 16 + kh * 8 + 2 * t);
-            const uint32_t ba0 = ba & 0xFFu, ba1 = ba >> 8, bb0 = bb & 0xFFu, bb1 = bb >> 8;
-            // signs of columns 16t + 0..15 of this half, as bf16 +-1 pairs
-            const uint32_t sa[8] = {sign_pair_bf16<0>(ba0), sign_pair_bf16<1>(ba0), sign_pair_bf16<2>(ba0),
-                                    sign_pair_bf16<3>(ba0), sign_pair_bf16<0>(ba1), sign_pair_bf16<1>(ba1),
-                                    sign_pair_bf16<2>(ba1), sign_pair_bf16<3>(ba1)};
-            const uint32_t sb[8] = {sign_pair_bf16<0>(bb0), sign_pair_bf16<1>(bb0), sign_pair_bf16<2>(bb0),
-                                    sign_pair_bf16<3>(bb0), sign_pair_bf16<0>(bb1), sign_pair_bf16<1>(bb1),
-                                    sign_pair_bf16<2>(bb1), sign_pair_bf16<3>(bb1)};
-            const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
-            const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
-            const uint8_t *xrow = st + L.x_off + kh * L.x_box + g * 128;
-            uint32_t xv[NT][8];
-#pragma unroll
-            for (int tt = 0; tt < NT; ++tt) {
-                const uint4 p0 = lds128(xrow + tt * 1024 + sw0);
-                const uint4 p1 = lds128(xrow + tt * 1024 + sw1);
-                xv[tt][0] = p0.x, xv[tt][1] = p0.y, xv[tt][2] = p0.z, xv[tt][3] = p0.w;
-                xv[tt][4] = p1.x, xv[tt][5] = p1.y, xv[tt][6] = p1.z, xv[tt][7] = p1.w;
-            }
-            // k-slice outer, tiles inner: consecutive MMAs never share an accumulator
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                for (int tt = 0; tt < NT; ++tt) {
-                    mma_bf16_16816(accb[tt], wa[2 * j], wb[2 * j], wa[2 * j + 1], wb[2 * j + 1], xv[tt][2 * j],
-                                   xv[tt][2 * j + 1]);
-                    mma_bf16_16816(accs[tt], sa[2 * j], sb[2 * j], sa[2 * j + 1], sb[2 * j + 1], xv[tt][2 * j],
-                                   xv[tt][2 * j + 1]);
-                }
-            }
+            dstage::consume_stage<NT>(smem + s * L.stage, L, kh, r0, g, t, sw, accb, accs);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
@@ -256,35 +199,10 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
         const float al0 = v0 ? (a.mode ? a.alpha[grow0] : a.alpha[0]) : 0.0f;
         const float al1 = v1 ? (a.mode ? a.alpha[grow0 + 8] : a.alpha[0]) : 0.0f;
         float part[NT][4];
-#pragma unroll
-        for (int tt = 0; tt < NT; ++tt) {
-            part[tt][0] = accb[tt][0] + al0 * accs[tt][0];
-            part[tt][1] = accb[tt][1] + al0 * accs[tt][1];
-            part[tt][2] = accb[tt][2] + al1 * accs[tt][2];
-            part[tt][3] = accb[tt][3] + al1 * accs[tt][3];
-        }
-        // red[token][row]: the upper half writes, the lower half adds its own and keeps the sum.
-        if (kh == 1) {
-#pragma unroll
-            for (int tt = 0; tt < NT; ++tt) {
-                const int c = 8 * tt + 2 * t;
-                red[c * rows + r0] = part[tt][0];
-                red[(c + 1) * rows + r0] = part[tt][1];
-                red[c * rows + r0 + 8] = part[tt][2];
-                red[(c + 1) * rows + r0 + 8] = part[tt][3];
-            }
-        }
+        dstage::fold_alpha<NT>(accb, accs, al0, al1, part);
+        if (kh == 1) dstage::halves_store<NT>(red, rows, r0, t, part);
         asm volatile("bar.sync 1, %0;" ::"n"(32 * n_cons) : "memory");  // consumer warps only
-        if (kh == 0) {
-#pragma unroll
-            for (int tt = 0; tt < NT; ++tt) {
-                const int c = 8 * tt + 2 * t;
-                red[c * rows + r0] += part[tt][0];
-                red[(c + 1) * rows + r0] += part[tt][1];
-                red[c * rows + r0 + 8] += part[tt][2];
-                red[(c + 1) * rows + r0 + 8] += part[tt][3];
-            }
-        }
+        if (kh == 0) dstage::halves_add<NT>(red, rows, r0, t, part);
     }
     cluster.sync();
 

@@ -154,6 +154,59 @@ int32_t bd_linear(const void *x, int64_t m, const void *w_base,
                   int64_t n_out, int64_t n_in, void *y, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * Batched fused linear  ([serve] fused linear, several independent
+ * projections per call -- e.g. q, k and v of a layer, or gate and up)
+ *
+ * Problem i computes exactly what bd_linear computes for descs[i].
+ * Problems with 1 <= m <= 16, n_in a multiple of 128 and x, w_base, bits
+ * and y 16-byte aligned are streamed together: up to
+ * BD_LINEAR_BATCH_PER_LAUNCH of them per launch (grouped by m <= 8 and
+ * m <= 16), with their work items -- one 128-column K step of one 64-row
+ * block -- split evenly over the resident CTAs.  A row block that several
+ * CTAs share is summed from fp32 partials in a fixed order, so results are
+ * deterministic; they may differ from bd_linear's in the last bits of fp32
+ * rounding (another split of K).  Every other problem, and a group that
+ * would hold a single problem, runs as bd_linear.
+ *
+ *   descs      host array [n] of bd_linear_desc (read during the call only;
+ *              `reserved` must be 0)
+ *   n          0 <= n <= BD_LINEAR_BATCH_MAX
+ *   workspace  device buffer of at least
+ *              bd_linear_batch_workspace_size(descs, n) bytes (the size
+ *              depends on the shapes and the current device), 256-byte
+ *              aligned and ZERO-FILLED before its first use.  Each call whose
+ *              kernels complete without a device error leaves it ready for the
+ *              next call (its block counters back at zero; the partial sums it
+ *              also holds need no clearing); after BD_ERR_DEVICE_TIMEOUT zero
+ *              it again before reuse.  Calls that may run concurrently need
+ *              distinct workspaces.  May be NULL when the size is 0.
+ *              Caller-owned.
+ * No y may overlap any input or another problem's y.  Ordered on `stream`.
+ * Errors: the first failing problem's bd_linear code (nothing launched),
+ *         BD_ERR_INVALID_ARG (n out of range, reserved != 0),
+ *         BD_ERR_WORKSPACE (missing, misaligned or too small), BD_ERR_CUDA;
+ *         BD_ERR_DEVICE_TIMEOUT later via bd_get_device_status.
+ * ------------------------------------------------------------------------ */
+#define BD_LINEAR_BATCH_MAX 256
+#define BD_LINEAR_BATCH_PER_LAUNCH 8
+typedef struct bd_linear_desc {
+    const void *x;        /* bf16 [m, n_in] */
+    const void *w_base;   /* bf16 [n_out, n_in] */
+    const uint8_t *bits;  /* uint8 [n_out, n_in/8] */
+    const float *alpha;   /* float [1] or [n_out] */
+    void *y;              /* bf16 [m, n_out] (written) */
+    int64_t m;
+    int64_t n_out;
+    int64_t n_in;
+    int32_t alpha_mode;
+    int32_t reserved;     /* 0 */
+} bd_linear_desc;
+
+size_t bd_linear_batch_workspace_size(const bd_linear_desc *descs, int32_t n);
+int32_t bd_linear_batch(const bd_linear_desc *descs, int32_t n, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Reconstruct-only pass ([serve]: W_eff = W_base + alpha * unpacked signs,
  * then a plain linear; [latency] reads decode as a standard matmul)
  *

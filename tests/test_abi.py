@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ["bd_compress", "bd_compress_workspace_size", "bd_linear", "bd_linear_grouped",
+    for required in ["bd_compress", "bd_compress_workspace_size", "bd_linear", "bd_linear_batch",
+                     "bd_linear_batch_workspace_size", "bd_linear_grouped",
                      "bd_linear_grouped_workspace_size", "bd_status_string", "bd_get_device_status"]:
         assert required in names
 
@@ -98,6 +99,41 @@ def test_linear_rejects_bad_arguments(lib):
     assert _linear(lib, alpha=MISALIGNED) == bd.BD_ERR_MISALIGNED
     # an empty batch is valid and launches nothing
     assert _linear(lib, m=0, x=0, y=0) == bd.BD_OK
+
+
+def _desc(**kw):
+    d = dict(x=ALIGNED, w_base=ALIGNED, bits=ALIGNED, alpha=ALIGNED, y=ALIGNED, m=4, n_out=64, n_in=256,
+             alpha_mode=0, reserved=0)
+    d.update(kw)
+    out = bd.LinearDesc()
+    for k, v in d.items():
+        setattr(out, k, v)
+    return out
+
+
+def _batch(lib, descs, ws=ALIGNED, ws_bytes=1 << 20, n=None):
+    arr = (bd.LinearDesc * len(descs))(*descs)
+    return lib.bd_linear_batch(arr, len(descs) if n is None else n, ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_linear_batch_rejects_bad_arguments(lib):
+    """Validation happens before any launch: every problem is checked as bd_linear checks it."""
+    good = _desc()
+    assert _batch(lib, [good, _desc(m=-1)]) == bd.BD_ERR_INVALID_ARG
+    assert _batch(lib, [good, _desc(x=0)]) == bd.BD_ERR_INVALID_ARG
+    assert _batch(lib, [_desc(alpha_mode=3)]) == bd.BD_ERR_INVALID_ARG
+    assert _batch(lib, [_desc(reserved=1)]) == bd.BD_ERR_INVALID_ARG
+    assert _batch(lib, [good, _desc(n_in=20)]) == bd.BD_ERR_UNSUPPORTED_SHAPE
+    assert _batch(lib, [_desc(y=MISALIGNED)]) == bd.BD_ERR_MISALIGNED
+    assert _batch(lib, [good], n=-1) == bd.BD_ERR_INVALID_ARG
+    assert _batch(lib, [good], n=bd.BD_LINEAR_BATCH_MAX + 1) == bd.BD_ERR_INVALID_ARG
+    assert lib.bd_linear_batch(None, 2, None, 0, None) == bd.BD_ERR_INVALID_ARG
+    # empty batches (no problems, or only m = 0 problems) are valid and launch nothing
+    assert _batch(lib, []) == bd.BD_OK
+    assert _batch(lib, [_desc(m=0, x=0, y=0)], ws=0, ws_bytes=0) == bd.BD_OK
+    arr = (bd.LinearDesc * 1)(_desc(m=-1))
+    assert lib.bd_linear_batch_workspace_size(arr, 1) == 0
+    assert lib.bd_linear_batch_workspace_size(None, 0) == 0
 
 
 def test_grouped_rejects_bad_arguments(lib):
