@@ -181,18 +181,31 @@ class Phase:
 
 
 def compress_phase(bd, mats, mode, dev):
-    """bd_compress over every (W_base, W_ft) of `mats`; outputs kept for the linear phases."""
-    calls, nbytes = [], 0.0
+    """Every (W_base, W_ft) of `mats` compressed -- in bd_compress_batch calls of up to 8
+    matrices (COMPRESS_BATCH), else one bd_compress per matrix; outputs kept for the
+    linear phases."""
+    calls, nbytes, launches = [], 0.0, 0
     outs = []
     for (wb, wf) in mats:
         n_out, n_in = wb.shape
         bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=dev)
         alpha = torch.empty((n_out if mode == 1 else 1,), dtype=torch.float32, device=dev)
-        ws = torch.empty((max(16, bd.bd_compress_workspace_size(n_out, n_in, mode)),), dtype=torch.uint8, device=dev)
-        calls.append(lambda wb=wb, wf=wf, bits=bits, alpha=alpha, ws=ws: bd.bd_compress(wb, wf, mode, bits, alpha, ws))
         nbytes += 4.0 * n_out * n_in + n_out * n_in / 8 + 4.0 * (n_out if mode == 1 else 1)
         outs.append((bits, alpha))
-    return Phase("compress", calls, bytes_=nbytes, launches=2 * len(mats)), outs
+        if not COMPRESS_BATCH:
+            ws = torch.empty((max(16, bd.bd_compress_workspace_size(n_out, n_in, mode)),), dtype=torch.uint8,
+                             device=dev)
+            calls.append(lambda wb=wb, wf=wf, bits=bits, alpha=alpha, ws=ws:
+                         bd.bd_compress(wb, wf, mode, bits, alpha, ws))
+            launches += 2
+    if COMPRESS_BATCH:
+        for i in range(0, len(mats), 8):
+            descs = bd.compress_descs([(wb, wf, mode, bits, alpha) for (wb, wf), (bits, alpha)
+                                       in zip(mats[i:i + 8], outs[i:i + 8])])
+            ws = torch.empty((max(256, bd.bd_compress_batch_workspace_size(descs)),), dtype=torch.uint8, device=dev)
+            calls.append(lambda descs=descs, ws=ws: bd.bd_compress_batch(descs, ws))
+            launches += 2
+    return Phase("compress", calls, bytes_=nbytes, launches=launches), outs
 
 
 # Fused linears of the device-resident decode/prefill phases are captured with
@@ -205,6 +218,9 @@ WEIGHT_PREFETCH = True
 # their input in a real layer -- q, k, v and gate, up -- to one bd_linear_batch call
 # each (o and down alone, through the same entry); "none" calls bd_linear per matrix.
 LINEAR_BATCH = "layer"
+# Compressions issued through bd_compress_batch (up to 8 matrices per call); --compress-batch 0
+# issues one bd_compress per matrix.
+COMPRESS_BATCH = True
 FUSED_GROUPS = ({"q", "k", "v"}, {"gate", "up"})
 
 
@@ -308,6 +324,7 @@ class LayerWorkload(Workload):
                        "matrix_count": len(shapes), "tokens": list(ms),
                        "alpha": "per-row" if mode == 1 else "scalar", "dtype_in": "bf16 weights/activations",
                        "weight_prefetch": WEIGHT_PREFETCH, "linear_batch": LINEAR_BATCH,
+                       "compress_batch": COMPRESS_BATCH,
                        "l2": "inputs larger than L2 (consecutive uses of a matrix separated by >250 MB of traffic)"}
 
     def oracle_sample(self, oracle, frac_rows: float):
@@ -735,6 +752,18 @@ class _NoLib:
     def bd_linear_grouped_workspace_size(self, *a):
         return 16
 
+    def bd_compress_batch_workspace_size(self, *a):
+        return 256
+
+    def bd_linear_batch_workspace_size(self, *a):
+        return 256
+
+    def compress_descs(self, problems):
+        return problems
+
+    def linear_descs(self, problems):
+        return problems
+
     def __getattr__(self, name):
         def _never(*a, **k):
             raise RuntimeError("the reference arm does not call the GPU library")
@@ -946,12 +975,15 @@ def main():
                     help="capture the device-resident fused linears with bd_set_weight_prefetch(1)")
     ap.add_argument("--linear-batch", choices=["none", "layer"], default="layer",
                     help="layer: q/k/v and gate/up of a layer in one bd_linear_batch call each")
+    ap.add_argument("--compress-batch", type=int, choices=[0, 1], default=1,
+                    help="compress through bd_compress_batch (8 matrices per call) or one bd_compress each")
     ap.add_argument("--kernel-case", default=None,
                     help="linear:N_OUTxN_IN:M[:path] or compress:N_OUTxN_IN[:mode] (one kernel, eager)")
     args = ap.parse_args()
-    global WEIGHT_PREFETCH, LINEAR_BATCH
+    global WEIGHT_PREFETCH, LINEAR_BATCH, COMPRESS_BATCH
     WEIGHT_PREFETCH = bool(args.weight_prefetch)
     LINEAR_BATCH = args.linear_batch
+    COMPRESS_BATCH = bool(args.compress_batch)
     if args.kernel_case:
         run_kernel_case(args)
         return

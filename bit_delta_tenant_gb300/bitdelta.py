@@ -31,6 +31,8 @@ BD_ALPHA_PER_ROW = 1
 BD_MAX_VARIANTS = 64
 BD_NOALLOC_MAX_PARTIALS = 131072
 BD_LINEAR_BATCH_MAX = 256
+BD_COMPRESS_BATCH_MAX = 4096
+BD_COMPRESS_BATCH_PER_LAUNCH = 8
 BD_LINEAR_BATCH_PER_LAUNCH = 8
 
 _lock = threading.Lock()
@@ -43,6 +45,13 @@ class LinearDesc(ctypes.Structure):
                 ("alpha", ctypes.c_void_p), ("y", ctypes.c_void_p), ("m", ctypes.c_int64),
                 ("n_out", ctypes.c_int64), ("n_in", ctypes.c_int64), ("alpha_mode", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class CompressDesc(ctypes.Structure):
+    """bd_compress_desc: one matrix of bd_compress_batch (device pointers and sizes)."""
+    _fields_ = [("w_base", ctypes.c_void_p), ("w_ft", ctypes.c_void_p), ("bits_out", ctypes.c_void_p),
+                ("alpha_out", ctypes.c_void_p), ("n_out", ctypes.c_int64), ("n_in", ctypes.c_int64),
+                ("alpha_mode", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class BitDeltaError(RuntimeError):
@@ -102,6 +111,10 @@ def load_library(path: str | None = None):
         lib.bd_compress_noalloc.restype = I32
         lib.bd_linear.argtypes = [V, I64, V, V, V, I32, I64, I64, V, V]
         lib.bd_linear.restype = I32
+        lib.bd_compress_batch_workspace_size.argtypes = [ctypes.POINTER(CompressDesc), I32]
+        lib.bd_compress_batch_workspace_size.restype = SZ
+        lib.bd_compress_batch.argtypes = [ctypes.POINTER(CompressDesc), I32, V, SZ, V]
+        lib.bd_compress_batch.restype = I32
         lib.bd_linear_batch_workspace_size.argtypes = [ctypes.POINTER(LinearDesc), I32]
         lib.bd_linear_batch_workspace_size.restype = SZ
         lib.bd_linear_batch.argtypes = [ctypes.POINTER(LinearDesc), I32, V, SZ, V]
@@ -261,6 +274,28 @@ def bd_linear(x: torch.Tensor, w_base: torch.Tensor, bits: torch.Tensor, alpha: 
     rc = load_library().bd_linear(_ptr(x), m, _ptr(w_base), _ptr(bits), _ptr(alpha), int(alpha_mode), n_out, n_in,
                                   _ptr(y), _stream(stream))
     _check(rc, "bd_linear")
+
+
+def compress_descs(problems) -> ctypes.Array:
+    """bd_compress_desc array from (w_base, w_ft, alpha_mode, bits_out, alpha_out) tuples of tensors."""
+    arr = (CompressDesc * len(problems))()
+    for d, (w_base, w_ft, alpha_mode, bits_out, alpha_out) in zip(arr, problems):
+        n_out, n_in = w_base.shape
+        d.w_base, d.w_ft, d.bits_out, d.alpha_out = (_ptr(w_base).value, _ptr(w_ft).value, _ptr(bits_out).value,
+                                                     _ptr(alpha_out).value)
+        d.n_out, d.n_in, d.alpha_mode, d.reserved = n_out, n_in, int(alpha_mode), 0
+    return arr
+
+
+def bd_compress_batch_workspace_size(descs: ctypes.Array) -> int:
+    return int(load_library().bd_compress_batch_workspace_size(descs, len(descs)))
+
+
+def bd_compress_batch(descs: ctypes.Array, workspace: torch.Tensor, stream=None) -> None:
+    """Each matrix's (bits, alpha) as bd_compress gives it, several matrices per launch."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().bd_compress_batch(descs, len(descs), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "bd_compress_batch")
 
 
 def linear_descs(problems) -> ctypes.Array:

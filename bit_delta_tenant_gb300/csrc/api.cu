@@ -196,6 +196,66 @@ BD_API int32_t bd_compress(const void *w_base, const void *w_ft, int64_t n_out, 
                                            static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+// Workspace offset of each matrix's partial sums in a batched compression (256-byte aligned regions).
+size_t compress_region(const bd_compress_desc &d) {
+    return (bd_compress_workspace_size(d.n_out, d.n_in, d.alpha_mode) + 255) / 256 * 256;
+}
+
+int32_t validate_compress_batch(const bd_compress_desc *d, int32_t n) {
+    if (n < 0 || n > BD_COMPRESS_BATCH_MAX) return BD_ERR_INVALID_ARG;
+    if (n > 0 && d == nullptr) return BD_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n; ++i) {
+        const bd_compress_desc &q = d[i];
+        if (q.reserved != 0) return BD_ERR_INVALID_ARG;
+        if (!q.w_base || !q.w_ft || !q.bits_out || !q.alpha_out) return BD_ERR_INVALID_ARG;
+        if (q.alpha_mode != BD_ALPHA_SCALAR && q.alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+        const int32_t shape = check_matrix_shape(q.n_out, q.n_in);
+        if (shape != BD_OK) return shape;
+        if (!aligned16(q.w_base) || !aligned16(q.w_ft) || !aligned16(q.bits_out) || !aligned16(q.alpha_out))
+            return BD_ERR_MISALIGNED;
+    }
+    return BD_OK;
+}
+
+}  // namespace
+
+BD_API size_t bd_compress_batch_workspace_size(const bd_compress_desc *descs, int32_t n) {
+    if (validate_compress_batch(descs, n) != BD_OK) return 0;
+    size_t need = 0;
+    for (int32_t i = 0; i < n; ++i) need += compress_region(descs[i]);
+    return need;
+}
+
+BD_API int32_t bd_compress_batch(const bd_compress_desc *descs, int32_t n, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+    const int32_t v = validate_compress_batch(descs, n);
+    if (v != BD_OK) return v;
+    if (n == 0) return BD_OK;
+    const size_t need = bd_compress_batch_workspace_size(descs, n);
+    if (workspace == nullptr || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return BD_ERR_WORKSPACE;
+    bd::DevCtx ctx;
+    const int32_t rc = make_ctx(&ctx);
+    if (rc != BD_OK) return rc;
+    std::vector<bd::CompressItem> items;
+    size_t off = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const bd_compress_desc &q = descs[i];
+        items.push_back({q.w_base, q.w_ft, q.n_out, q.n_in, q.alpha_mode, q.bits_out, q.alpha_out,
+                         reinterpret_cast<double *>(static_cast<uint8_t *>(workspace) + off)});
+        off += compress_region(q);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (size_t first = 0; first < items.size(); first += bd::kCompressBatchPerLaunch) {
+        const int count = static_cast<int>(std::min(items.size() - first, static_cast<size_t>(bd::kCompressBatchPerLaunch)));
+        const int32_t r = cuda_status(bd::launch_compress_batch(items.data() + first, count, ctx, s));
+        if (r != BD_OK) return r;
+    }
+    return BD_OK;
+}
+
 // ---------------------------------------------------------------- fused linear
 
 namespace {

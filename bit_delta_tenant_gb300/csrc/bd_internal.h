@@ -44,6 +44,22 @@ CompressGeom compress_geometry(int64_t n_out, int64_t n_in, int32_t alpha_mode);
 cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out, int64_t n_in, int32_t alpha_mode,
                             uint8_t *bits, float *alpha, double *partials, const DevCtx &ctx, cudaStream_t stream);
 
+// Several compressions in one launch of pass 1 (and one of pass 2): at most
+// kCompressBatchPerLaunch matrices, each with its own partials region (the
+// sizes bd_compress_workspace_size gives); same bits and alpha as one
+// launch_compress per matrix.
+constexpr int kCompressBatchPerLaunch = 8;
+struct CompressItem {
+    const void *w_base;
+    const void *w_ft;
+    int64_t n_out, n_in;
+    int32_t alpha_mode;
+    uint8_t *bits;
+    float *alpha;
+    double *partials;
+};
+cudaError_t launch_compress_batch(const CompressItem *items, int n, const DevCtx &ctx, cudaStream_t stream);
+
 // ---- fused linear ---------------------------------------------------------------------
 // HBM-streaming small-m kernel (m <= kDecodeMaxM).  Returns cudaErrorNotSupported
 // if the activation slice does not fit in shared memory (caller falls back).

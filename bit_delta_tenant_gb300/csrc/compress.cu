@@ -237,13 +237,10 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
 // reads in flight), writes their bytes and adds the four chunk sums, the warp
 // tree and the warps in exactly the order of the ring form above, so the
 // partials and alpha are the same bits.
-__global__ void __launch_bounds__(kCompressThreads) compress_direct(const __grid_constant__ CompressArgs a) {
-    pdl_trigger_and_wait();
-    __shared__ double warp_sum[kCompressThreads / 32];
+__device__ __forceinline__ void compress_segment(const CompressArgs &a, int64_t sg, double *warp_sum) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int64_t sg = blockIdx.x;
     const int64_t row = sg / a.segs;
     const int64_t first = (sg - row * a.segs) * kCompressChunksPerSeg;
     const int64_t n = min(static_cast<int64_t>(kCompressChunksPerSeg), a.row_chunks - first);
@@ -294,29 +291,48 @@ __global__ void __launch_bounds__(kCompressThreads) compress_direct(const __grid
     }
 }
 
+__global__ void __launch_bounds__(kCompressThreads) compress_direct(const __grid_constant__ CompressArgs a) {
+    pdl_trigger_and_wait();
+    __shared__ double warp_sum[kCompressThreads / 32];
+    compress_segment(a, blockIdx.x, warp_sum);
+}
+
+// Several matrices in one launch: block b takes segment b - first_block[p] of
+// matrix p (the largest p with first_block[p] <= b); the same per-segment
+// arithmetic, so bits and alpha equal those of one launch per matrix.
+struct CompressBatchArgs {
+    CompressArgs m[kCompressBatchPerLaunch];
+    int64_t first_block[kCompressBatchPerLaunch];
+    int32_t n;
+};
+
+__global__ void __launch_bounds__(kCompressThreads)
+    compress_direct_batch(const __grid_constant__ CompressBatchArgs a) {
+    pdl_trigger_and_wait();
+    __shared__ double warp_sum[kCompressThreads / 32];
+    const int64_t b = blockIdx.x;
+    int p = 0;
+    while (p + 1 < a.n && a.first_block[p + 1] <= b) ++p;
+    compress_segment(a.m[p], b - a.first_block[p], warp_sum);
+}
+
 // Pass 2 is launched as a programmatic dependent of pass 1: its CTAs become
 // resident while pass 1 streams and wait (griddepcontrol.wait) until pass 1
 // has completed and its partials are visible.
 
 // One thread per row (few segments per row): alpha_j = sum(partials)/count.
-__global__ void compress_pass2_rows(const double *partials, int64_t rows, int64_t segs, double count,
-                                    float *alpha) {
-    pdl_trigger_and_wait();
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (r >= rows) return;
+__device__ __forceinline__ void pass2_row(const double *partials, int64_t r, int64_t segs, double count,
+                                          float *alpha) {
     double s = 0.0;
     for (int64_t i = 0; i < segs; ++i) s += partials[r * segs + i];
     alpha[r] = static_cast<float>(s / count);
 }
 
-// One block per row (many segments): strided per-thread sums, then a fixed tree.
-__global__ void __launch_bounds__(256) compress_pass2_block(const double *partials, int64_t segs, double count,
-                                                            float *alpha) {
-    pdl_trigger_and_wait();
-    const int64_t r = blockIdx.x;
+// One 256-thread block per row (many segments): strided per-thread sums, then a fixed tree.
+__device__ __forceinline__ void pass2_block_row(const double *partials, int64_t r, int64_t segs, double count,
+                                                float *alpha, double *red) {
     double s = 0.0;
     for (int64_t i = threadIdx.x; i < segs; i += 256) s += partials[r * segs + i];
-    __shared__ double red[256];
     red[threadIdx.x] = s;
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
@@ -324,6 +340,50 @@ __global__ void __launch_bounds__(256) compress_pass2_block(const double *partia
         __syncthreads();
     }
     if (threadIdx.x == 0) alpha[r] = static_cast<float>(red[0] / count);
+}
+
+__global__ void compress_pass2_rows(const double *partials, int64_t rows, int64_t segs, double count,
+                                    float *alpha) {
+    pdl_trigger_and_wait();
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (r < rows) pass2_row(partials, r, segs, count, alpha);
+}
+
+__global__ void __launch_bounds__(256) compress_pass2_block(const double *partials, int64_t segs, double count,
+                                                            float *alpha) {
+    pdl_trigger_and_wait();
+    __shared__ double red[256];
+    pass2_block_row(partials, blockIdx.x, segs, count, alpha, red);
+}
+
+// Pass 2 of several matrices in one launch (256 threads): matrix p owns blocks
+// [first_block[p], first_block[p+1]); with at most kPass2RowsMaxSegs segments per
+// row each thread of its blocks sums one row, otherwise each block sums one row.
+// The per-row orders are those of the two kernels above.
+constexpr int64_t kPass2RowsMaxSegs = 32;
+struct Pass2BatchArgs {
+    const double *partials[kCompressBatchPerLaunch];
+    float *alpha[kCompressBatchPerLaunch];
+    int64_t rows[kCompressBatchPerLaunch];
+    int64_t segs[kCompressBatchPerLaunch];
+    double count[kCompressBatchPerLaunch];
+    int64_t first_block[kCompressBatchPerLaunch];
+    int32_t n;
+};
+
+__global__ void __launch_bounds__(256) compress_pass2_batch(const __grid_constant__ Pass2BatchArgs a) {
+    pdl_trigger_and_wait();
+    __shared__ double red[256];
+    const int64_t b = blockIdx.x;
+    int p = 0;
+    while (p + 1 < a.n && a.first_block[p + 1] <= b) ++p;
+    const int64_t lb = b - a.first_block[p];
+    if (a.segs[p] <= kPass2RowsMaxSegs) {
+        const int64_t r = lb * 256 + threadIdx.x;
+        if (r < a.rows[p]) pass2_row(a.partials[p], r, a.segs[p], a.count[p], a.alpha[p]);
+    } else {
+        pass2_block_row(a.partials[p], lb, a.segs[p], a.count[p], a.alpha[p], red);
+    }
 }
 
 }  // namespace
@@ -389,7 +449,7 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
     c2.stream = stream;
     c2.attrs = attr;
     c2.numAttrs = 1;
-    if (g.segs <= 32) {
+    if (g.segs <= kPass2RowsMaxSegs) {
         c2.gridDim = dim3(static_cast<unsigned>((g.rows + 127) / 128), 1, 1);
         c2.blockDim = dim3(128, 1, 1);
         return cudaLaunchKernelEx(&c2, compress_pass2_rows, static_cast<const double *>(partials), g.rows, g.segs,
@@ -398,6 +458,61 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
     c2.gridDim = dim3(static_cast<unsigned>(g.rows), 1, 1);
     c2.blockDim = dim3(256, 1, 1);
     return cudaLaunchKernelEx(&c2, compress_pass2_block, static_cast<const double *>(partials), g.segs, count, alpha);
+}
+
+}  // namespace bd
+
+namespace bd {
+
+cudaError_t launch_compress_batch(const CompressItem *items, int n, const DevCtx &ctx, cudaStream_t stream) {
+    if (n < 1 || n > kCompressBatchPerLaunch) return cudaErrorInvalidValue;
+    CompressBatchArgs a1{};
+    Pass2BatchArgs a2{};
+    int64_t blocks1 = 0, blocks2 = 0;
+    int n2 = 0;
+    for (int i = 0; i < n; ++i) {
+        const CompressItem &it = items[i];
+        const CompressGeom g = compress_geometry(it.n_out, it.n_in, it.alpha_mode);
+        CompressArgs &a = a1.m[i];
+        a.wb = static_cast<const uint4 *>(it.w_base);
+        a.wf = static_cast<const uint4 *>(it.w_ft);
+        a.bits = it.bits;
+        a.partials = it.partials;
+        a.alpha = it.alpha;
+        a.count = static_cast<double>(g.row_chunks) * 8.0;
+        a.row_chunks = g.row_chunks;
+        a.segs = g.segs;
+        a1.first_block[i] = blocks1;
+        blocks1 += g.rows * g.segs;
+        if (g.segs > 1) {  // pass 2 only for rows split into several segments
+            a2.partials[n2] = it.partials;
+            a2.alpha[n2] = it.alpha;
+            a2.rows[n2] = g.rows;
+            a2.segs[n2] = g.segs;
+            a2.count[n2] = a.count;
+            a2.first_block[n2] = blocks2;
+            blocks2 += g.segs <= kPass2RowsMaxSegs ? (g.rows + 255) / 256 : g.rows;
+            ++n2;
+        }
+    }
+    a1.n = n;
+    a2.n = n2;
+    if (blocks1 > 0x7FFFFFFFLL || blocks2 > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks1), 1, 1);
+    cfg.blockDim = dim3(kCompressThreads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, compress_direct_batch, a1);
+    if (e != cudaSuccess || n2 == 0) return e;
+    cudaLaunchConfig_t c2 = cfg;
+    c2.gridDim = dim3(static_cast<unsigned>(blocks2), 1, 1);
+    c2.blockDim = dim3(256, 1, 1);
+    return cudaLaunchKernelEx(&c2, compress_pass2_batch, a2);
 }
 
 }  // namespace bd

@@ -101,6 +101,45 @@ int32_t bd_compress(const void *w_base, const void *w_ft, int64_t n_out,
                     void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * Batched compression  ([math], [infra]: every matrix of a fine-tune is
+ * compressed against its base)
+ *
+ * Matrix i gets exactly the bits and alpha bd_compress gives it (same
+ * per-segment arithmetic and summation order), with up to
+ * BD_COMPRESS_BATCH_PER_LAUNCH matrices per launch of each pass instead of
+ * two launches per matrix.
+ *
+ *   descs      host array [n] of bd_compress_desc (read during the call only;
+ *              `reserved` must be 0); each as in bd_compress
+ *   n          0 <= n <= BD_COMPRESS_BATCH_MAX
+ *   workspace  device scratch of at least
+ *              bd_compress_batch_workspace_size(descs, n) bytes (each
+ *              matrix's bd_compress_workspace_size, rounded up to 256 bytes),
+ *              256-byte aligned; its contents on entry are ignored.
+ * Ordered on `stream`; buffers caller-owned.  No output may overlap an input
+ * or another matrix's output.
+ * Errors: the first failing matrix's bd_compress code (nothing launched),
+ *         BD_ERR_INVALID_ARG (n out of range, reserved != 0),
+ *         BD_ERR_WORKSPACE, BD_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+#define BD_COMPRESS_BATCH_MAX 4096
+#define BD_COMPRESS_BATCH_PER_LAUNCH 8
+typedef struct bd_compress_desc {
+    const void *w_base;   /* bf16 [n_out, n_in] */
+    const void *w_ft;     /* bf16 [n_out, n_in] */
+    uint8_t *bits_out;    /* uint8 [n_out, n_in/8] (written) */
+    float *alpha_out;     /* float [1] or [n_out] (written) */
+    int64_t n_out;
+    int64_t n_in;
+    int32_t alpha_mode;
+    int32_t reserved;     /* 0 */
+} bd_compress_desc;
+
+size_t bd_compress_batch_workspace_size(const bd_compress_desc *descs, int32_t n);
+int32_t bd_compress_batch(const bd_compress_desc *descs, int32_t n, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Compression without a workspace.  The page has no counterpart to this
  * entry point; it exists for callers that cannot hand the library any device
  * memory besides the inputs and outputs -- for example code running under a

@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for required in ["bd_compress", "bd_compress_workspace_size", "bd_linear", "bd_linear_batch",
+    for required in ["bd_compress", "bd_compress_workspace_size", "bd_compress_batch",
+                     "bd_compress_batch_workspace_size", "bd_linear", "bd_linear_batch",
                      "bd_linear_batch_workspace_size", "bd_linear_grouped",
                      "bd_linear_grouped_workspace_size", "bd_status_string", "bd_get_device_status"]:
         assert required in names
@@ -114,6 +115,36 @@ def _desc(**kw):
 def _batch(lib, descs, ws=ALIGNED, ws_bytes=1 << 20, n=None):
     arr = (bd.LinearDesc * len(descs))(*descs)
     return lib.bd_linear_batch(arr, len(descs) if n is None else n, ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def _cdesc(**kw):
+    d = dict(w_base=ALIGNED, w_ft=ALIGNED, bits_out=ALIGNED, alpha_out=ALIGNED, n_out=64, n_in=256,
+             alpha_mode=0, reserved=0)
+    d.update(kw)
+    out = bd.CompressDesc()
+    for k, v in d.items():
+        setattr(out, k, v)
+    return out
+
+
+def test_compress_batch_rejects_bad_arguments(lib):
+    def call(descs, ws=ALIGNED, ws_bytes=1 << 20, n=None):
+        arr = (bd.CompressDesc * len(descs))(*descs)
+        return lib.bd_compress_batch(arr, len(descs) if n is None else n, ctypes.c_void_p(ws), ws_bytes, None)
+    good = _cdesc()
+    assert call([good, _cdesc(w_ft=0)]) == bd.BD_ERR_INVALID_ARG
+    assert call([_cdesc(alpha_mode=2)]) == bd.BD_ERR_INVALID_ARG
+    assert call([_cdesc(reserved=5)]) == bd.BD_ERR_INVALID_ARG
+    assert call([good, _cdesc(n_in=12)]) == bd.BD_ERR_UNSUPPORTED_SHAPE
+    assert call([_cdesc(bits_out=MISALIGNED)]) == bd.BD_ERR_MISALIGNED
+    assert call([good], n=bd.BD_COMPRESS_BATCH_MAX + 1) == bd.BD_ERR_INVALID_ARG
+    assert call([good], ws=0) == bd.BD_ERR_WORKSPACE
+    assert call([good], ws=ALIGNED + 16) == bd.BD_ERR_WORKSPACE      # not 256-byte aligned
+    assert call([good], ws_bytes=8) == bd.BD_ERR_WORKSPACE
+    assert call([]) == bd.BD_OK
+    arr = (bd.CompressDesc * 2)(good, _cdesc(alpha_mode=1, n_out=3, n_in=16392))
+    # scalar 64x256: 2 segments; per-row 16392: 3 segments per row; each region rounded to 256 bytes
+    assert lib.bd_compress_batch_workspace_size(arr, 2) == 256 + 256
 
 
 def test_linear_batch_rejects_bad_arguments(lib):

@@ -129,3 +129,69 @@ def test_zero_delta_packs_all_ones_and_alpha_zero():
     bits, alpha = gpu_compress(w_base, w_base.clone(), 1)
     assert torch.all(bits == 255)
     assert torch.all(alpha == 0)
+
+
+def gpu_compress_batch(mats):
+    """bd_compress_batch over [(w_base, w_ft, mode)]; returns [(bits, alpha)]."""
+    outs, probs = [], []
+    for w_base, w_ft, mode in mats:
+        n_out, n_in = w_base.shape
+        bits = torch.full((n_out, n_in // 8), 0xAA, dtype=torch.uint8, device=w_base.device)
+        alpha = torch.full((n_out if mode == 1 else 1,), float("nan"), dtype=torch.float32, device=w_base.device)
+        outs.append((bits, alpha))
+        probs.append((w_base, w_ft, mode, bits, alpha))
+    descs = bd.compress_descs(probs)
+    ws = torch.empty((max(1, bd.bd_compress_batch_workspace_size(descs)),), dtype=torch.uint8, device="cuda")
+    bd.bd_compress_batch(descs, ws)
+    torch.cuda.synchronize()
+    return outs
+
+
+BATCH_SHAPES = [  # scalar (many segments: block pass 2), per-row one segment, per-row 2..32 segments, ragged
+    (256, 512, 0), (33, 120, 1), (3, 16392, 1), (129, 136, 0), (1000, 8192, 1), (7, 24, 0), (64, 65536, 1),
+    (300, 4096, 0), (1, 8, 1), (2048, 11008, 0),
+]
+
+
+@pytest.mark.parametrize("count", [1, 3, 8, 10])
+def test_batched_compression_equals_single_calls_and_oracle(count):
+    """Every matrix of a batch gets the bits and alpha of its own bd_compress call (bitwise), and the
+    oracle's bits and alpha; 10 matrices take two launches of each pass."""
+    mats = []
+    for i, (n_out, n_in, mode) in enumerate(BATCH_SHAPES[:count]):
+        w_base, w_ft = synth.matrix_pair(n_out, n_in, 0.02, 1e-3, seed=40 + i, device="cuda")
+        mats.append((w_base, w_ft, mode))
+    outs = gpu_compress_batch(mats)
+    for i, ((w_base, w_ft, mode), (bits, alpha)) in enumerate(zip(mats, outs)):
+        b1, a1 = check_against_oracle(w_base, w_ft, mode)
+        assert torch.equal(bits, b1), f"matrix {i}: bits differ from bd_compress"
+        assert torch.equal(alpha.view(torch.int32), a1.view(torch.int32)), f"matrix {i}: alpha differs"
+
+
+def test_batched_compression_of_the_llama7b_layer():
+    c = workloads.LLAMA7B_LAYER
+    mats = []
+    for i, (_, n_out, n_in) in enumerate(c["matrices"]):
+        w_base, w_ft = synth.matrix_pair(n_out, n_in, c["sigma"], c["b"], workloads.matrix_seed(c["seed"], i), "cuda")
+        mats.append((w_base, w_ft, c["mode"]))
+    outs = gpu_compress_batch(mats)
+    for (w_base, w_ft, mode), (bits, alpha) in zip(mats, outs):
+        b1, a1 = gpu_compress(w_base, w_ft, mode)
+        assert torch.equal(bits, b1)
+        assert torch.equal(alpha.view(torch.int32), a1.view(torch.int32))
+        wb, wf = synth.as_u16(w_base), synth.as_u16(w_ft)
+        a64 = oracle.alpha(wb, wf, mode)
+        assert abs(float(alpha[0]) - a64[0]) / abs(a64[0]) <= ALPHA_REL
+
+
+def test_batched_compression_workspace_errors():
+    w_base, w_ft = synth.matrix_pair(64, 8192, 0.02, 1e-3, seed=3, device="cuda")
+    bits = torch.empty((64, 1024), dtype=torch.uint8, device="cuda")
+    alpha = torch.empty((1,), dtype=torch.float32, device="cuda")
+    descs = bd.compress_descs([(w_base, w_ft, 0, bits, alpha)])
+    need = bd.bd_compress_batch_workspace_size(descs)
+    assert need == (bd.bd_compress_workspace_size(64, 8192, 0) + 255) // 256 * 256
+    with pytest.raises(bd.BitDeltaError) as e:
+        bd.bd_compress_batch(descs, torch.empty(need - 256, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == bd.BD_ERR_WORKSPACE
+    assert bd.bd_compress_batch_workspace_size((bd.CompressDesc * 0)()) == 0
