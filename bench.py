@@ -210,8 +210,9 @@ def compress_phase(bd, mats, mode, dev):
 
 # Fused linears of the device-resident decode/prefill phases are captured with
 # bd_set_weight_prefetch(1) (static weights, as when serving); --weight-prefetch 0
-# turns it off.  The end-to-end leg always runs with the library default (off),
-# since there a linear follows the compression that writes its bits.
+# turns it off.  The end-to-end leg replays the same graphs: a graph launch starts
+# only after the previous one (the compression that writes the bits) has completed,
+# and inside the linear graph no kernel writes weights.
 WEIGHT_PREFETCH = True
 
 # How a layer's fused linears are issued: "layer" passes the projections that share

@@ -396,7 +396,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-int stages_for(int nt) { return nt == 1 ? 5 : 4; }
+// Ring depth: the deepest that keeps two CTAs per SM (BD_BATCH_STAGES overrides, for sweeps).
+int stages_for(int nt) {
+    static const int forced = [] {
+        const char *e = std::getenv("BD_BATCH_STAGES");
+        return e != nullptr ? std::atoi(e) : 0;
+    }();
+    if (forced >= 2 && forced <= 12) return forced;
+    return nt == 1 ? 5 : 4;
+}
 
 size_t smem_for(int nt) {
     const StageLayout L = stage_layout(kRG, nt);
