@@ -26,6 +26,8 @@
 // through distributed shared memory, then written to the original token rows.
 #include <cooperative_groups.h>
 
+#include <cstdlib>
+
 #include "bd_device.cuh"
 #include "bd_internal.h"
 
@@ -448,10 +450,25 @@ cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w
     a.status = ctx.status;
     a.wait_ns = ctx.wait_ns;
     for (int i = 0; i < 4; ++i) a.sign_mul[i] = (1u << (15 - 2 * i)) + (1u << (30 - 2 * i));
-    // K split over a cluster when the 64-row blocks leave SMs idle (one CTA per SM here).
+    // K split over a cluster of c CTAs (one CTA per SM here): the c in 1..8 that minimises
+    // waves x (K steps per CTA + a CTA's fixed cost of about 3 steps),
+    // ceil(blocks * c / SMs) * (ceil(steps / c) + 3), the smallest on ties, with clusters above
+    // four CTAs only when they fit in one wave (their scheduling costs more).  Fitted to GB300
+    // measurements at 64 tokens, 14 variants: 14336 x 4096 164 us with c = 2 against 195 us
+    // with c = 1; 4096 x 4096 61 us (c = 2) against 81 us (c = 3); 8192 x 8192 186 us (c = 1)
+    // against 195 / 206 / 255 us (c = 2 / 4 / 8).
     const int64_t row_blocks = (n_out + kRows - 1) / kRows;
     const int64_t steps = n_in / kStepK;
-    int64_t c = row_blocks >= ctx.num_sms ? 1 : (ctx.num_sms + row_blocks - 1) / row_blocks;
+    int64_t c = 1, best = -1;
+    for (int64_t cc = 1; cc <= 8 && cc <= steps; ++cc) {
+        if (cc > 4 && row_blocks * cc > ctx.num_sms) continue;  // clusters above 4 only in a single wave
+        const int64_t cost = (row_blocks * cc + ctx.num_sms - 1) / ctx.num_sms * ((steps + cc - 1) / cc + 3);
+        if (best < 0 || cost < best) best = cost, c = cc;
+    }
+    if (const char *e = std::getenv("BD_GROUPED_CLUSTER")) {  // sweeps
+        const int64_t v = std::atoll(e);
+        if (v >= 1) c = v;
+    }
     if (c > 8) c = 8;
     if (c > steps) c = steps;
     const int64_t per = (steps + c - 1) / c;
