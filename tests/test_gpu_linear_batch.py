@@ -152,6 +152,22 @@ def test_llama7b_layer_batches_full_size(m):
         assert_reusable(cases, ys, ws, f"{group} m={m}")
 
 
+@pytest.mark.parametrize("m", [1, 9])
+def test_llama3_8b_qkv_batch_full_size_per_row_alpha(m):
+    """q (4096 x 4096) with k and v (1024 x 4096) in one batch, per-row alpha, sampled outputs."""
+    shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
+    cases = [LinearCase(n_out, n_in, m, 0.02, 1e-3, 1, seed=750 + i) for i, (n_out, n_in) in enumerate(shapes)]
+    ys, ws = run_batch(cases)
+    torch.cuda.synchronize()
+    assert bd.bd_get_device_status() == bd.BD_OK
+    for i, (case, y) in enumerate(zip(cases, ys)):
+        yh = y_host(y)
+        ts, js = sample_outputs(case.m, case.n_out, 400, seed=10 + i)
+        y_ref, mag = case.reference_sampled(ts, js)
+        assert_y_close(yh[ts, js], y_ref, mag, f"qkv problem {i} m={m}")
+    assert_reusable(cases, ys, ws, f"qkv m={m}")
+
+
 def test_in_a_graph_with_weight_prefetch_and_a_dependent_batch():
     """Two batches captured in a graph with weight prefetch on; the second batch
     reads the first one's output as its activations (a read-after-write that a
