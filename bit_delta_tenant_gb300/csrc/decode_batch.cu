@@ -26,12 +26,11 @@
 // half) and one TMA producer warp, as in decode_tma.cu, plus an epilogue warp:
 // at the end of its part of a row block the consumers add their K halves into
 // one of two shared-memory buffers and go on with the next block's stages,
-// while the epilogue warp writes y (or the partial, the counter and, for the
-// CTA that completes the block, the sum), so the ring never waits on global
-// memory round trips.  Launches allow
-// programmatic dependent launch; with weight prefetch enabled the first
-// stages' W_base and bits boxes are issued before griddepcontrol.wait, every
-// other global access after it.
+// while the epilogue warp writes y -- or publishes the partial and counts it,
+// or, in the block's owner, adds the partials -- so the ring never waits on
+// global memory round trips.  Launches allow programmatic dependent launch;
+// with weight prefetch enabled the first stages' W_base and bits boxes are
+// issued before griddepcontrol.wait, every other global access after it.
 #include <cstdlib>
 
 #include "bd_internal.h"
