@@ -715,6 +715,9 @@ def cpu_baseline(wl, args, target_s: float = 12.0):
             "sample": desc, "seconds": dt}
 
 
+REFERENCE_BUDGET_S = 90.0
+
+
 def run_reference(args, ws, rank):
     """The fp64 CPU oracle as it stands, on the host cores; rank 0 only."""
     if rank != 0:
@@ -724,8 +727,19 @@ def run_reference(args, ws, rank):
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     from bit_delta_tenant_gb300 import bitdelta as bd  # noqa: F401  (workload construction only)
     wl = WORKLOADS[args.workload](_NoLib(), dev)
+    # Each step is the largest row sample (up to the whole step) that keeps the run near
+    # REFERENCE_BUDGET_S: one 1/64 sample is timed first and scaled.
     frac = 1.0 / 64
     run, desc = wl.oracle_sample(oracle, frac)
+    t0 = time.perf_counter()
+    run()
+    t_small = time.perf_counter() - t0
+    budget_frac = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup) / max(t_small, 1e-4) * frac
+    if budget_frac > frac:
+        frac = min(1.0, budget_frac)
+        run, desc = wl.oracle_sample(oracle, frac)
+        if frac >= 1.0:
+            desc = desc.replace("each matrix's first 1 of rows", "every row of every matrix")
     for _ in range(args.warmup):
         run()
     t0 = time.perf_counter()
