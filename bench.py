@@ -286,13 +286,16 @@ class LayerWorkload(Workload):
         groups = layer_groups([n for n, _, _ in shapes]) if LINEAR_BATCH == "layer" else \
             [[i] for i in range(len(shapes))]
         self.batch_ws = None
+        self.linear_plan = []  # (matrices the call needs, call) for the pipelined end-to-end step
         for m in ms:
             for grp in groups:
                 probs = []
-                for i in grp:
+                for j, i in enumerate(grp):
                     _, n_out, n_in = shapes[i]
                     xk = (m, i) if private_io else (m, n_in)
-                    yk = (m, i) if private_io else (m, n_out)
+                    # shared outputs are reused across calls, never within one (bd_linear_batch's
+                    # problems may not share a y)
+                    yk = (m, i) if private_io else (m, n_out, j)
                     if xk not in self.xs:
                         self.xs[xk] = synth.activations(m, n_in, 10_000 + 97 * len(self.xs) + m, dev)
                     if yk not in self.ys:
@@ -314,11 +317,18 @@ class LayerWorkload(Workload):
                     calls.append(lambda x=x, wb=wb, bits=bits, alpha=alpha, y=y:
                                  bd.bd_linear(x, wb, bits, alpha, mode, y))
                     launches += 1
+                self.linear_plan.append((set(grp), calls[-1]))
         bound = "hbm" if unit == "GB/s" else "tensor"
         self.lin = Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=launches, bound=bound,
                          weight_prefetch=WEIGHT_PREFETCH)
         self.phases = [self.comp, self.lin]
         self.dominant = self.lin
+        # one compression call per matrix, for the pipelined end-to-end step
+        self.compress_one = []
+        for (wb, wf), (bits, alpha) in zip(self.mats, self.packed):
+            descs = bd.compress_descs([(wb, wf, mode, bits, alpha)])
+            ws = torch.empty((max(256, bd.bd_compress_batch_workspace_size(descs)),), dtype=torch.uint8, device=dev)
+            self.compress_one.append(lambda descs=descs, ws=ws: bd.bd_compress_batch(descs, ws))
         self.h2d_tensors = [wf for (_, wf) in self.mats] + list(self.xs.values())
         self.d2h_tensors = list(self.ys.values()) + [a for (_, a) in self.packed]
         self.config = {"workload": name, "matrices": sorted({f"{a}x{b}" for _, a, b in shapes}),
@@ -650,19 +660,61 @@ def lookup_traffic(workload: str, phase):
     return float(m.group(1))
 
 
+def pipelined_step(wl, h2d, d2h, stream, copy_stream):
+    """One end-to-end step of a layer workload with the host copies overlapped: the
+    activations, then each matrix's W_ft, go up on `copy_stream`; on `stream` each matrix
+    is compressed as soon as its W_ft has landed, and each linear call is issued as soon as
+    the matrices it reads are compressed (weight prefetch off: a linear may directly follow
+    the compression of its bits).  Then the outputs come back."""
+    n = len(wl.mats)
+    ev = [torch.cuda.Event() for _ in range(n)]
+    ex = torch.cuda.Event()
+
+    def one():
+        copy_stream.wait_stream(stream)  # the previous step has finished with these buffers
+        with torch.cuda.stream(copy_stream):
+            for host, devt in h2d[n:]:
+                devt.copy_(host, non_blocking=True)
+            ex.record(copy_stream)
+            for i in range(n):
+                h2d[i][1].copy_(h2d[i][0], non_blocking=True)
+                ev[i].record(copy_stream)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ex)
+            issued = [False] * len(wl.linear_plan)
+            done = set()
+            for i in range(n):
+                stream.wait_event(ev[i])
+                wl.compress_one[i]()
+                done.add(i)
+                for k, (need, call) in enumerate(wl.linear_plan):
+                    if not issued[k] and need <= done:
+                        call()
+                        issued[k] = True
+            for host, devt in d2h:
+                host.copy_(devt, non_blocking=True)
+    return one
+
+
 def run_e2e(args, wl, stream, ws):
-    """Same step through the C ABI with host buffers: H2D of the step's inputs, kernels, D2H of results."""
+    """Same step through the C ABI with host buffers: H2D of the step's inputs, kernels, D2H of
+    results.  Layer workloads overlap the copies with the compressions and linears
+    (pipelined_step); the others copy, replay the step's graphs and copy back."""
     h2d, d2h = wl.e2e_buffers()
     bi = sum(t.numel() * t.element_size() for t, _ in h2d)
     bo = sum(t.numel() * t.element_size() for t, _ in d2h)
+    pipelined = hasattr(wl, "linear_plan")
 
-    def one():
-        for host, devt in h2d:
-            devt.copy_(host, non_blocking=True)
-        for p in wl.phases:
-            p.replay()
-        for host, devt in d2h:
-            host.copy_(devt, non_blocking=True)
+    if pipelined:
+        one = pipelined_step(wl, h2d, d2h, stream, torch.cuda.Stream())
+    else:
+        def one():
+            for host, devt in h2d:
+                devt.copy_(host, non_blocking=True)
+            for p in wl.phases:
+                p.replay()
+            for host, devt in d2h:
+                host.copy_(devt, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(1, args.warmup)):
@@ -677,8 +729,19 @@ def run_e2e(args, wl, stream, ws):
         e.record(stream)
     torch.cuda.synchronize()
     t = max_over_ranks(ws, s.elapsed_time(e))
+    if pipelined:
+        # the overlapped step must give the graph-replayed step's results, bit for bit
+        got = [host.clone() for host, _ in d2h]
+        with torch.cuda.stream(stream):
+            for p in wl.phases:
+                p.replay()
+        torch.cuda.synchronize()
+        for g, (_, devt) in zip(got, d2h):
+            if not torch.equal(g, devt.cpu()):
+                raise RuntimeError("end-to-end step and device-resident step disagree")
     return {"value": ws * args.steps * wl.step_work() / (t * 1e-3) / 1e9, "unit": wl.metric_unit,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": t / args.steps}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": t / args.steps,
+            "copies": "overlapped with the compressions and linears" if pipelined else "before the step"}
 
 
 def cpu_cores():
