@@ -221,6 +221,11 @@ int32_t bd_linear(const void *x, int64_t m, const void *w_base,
  *              distinct workspaces.  May be NULL when the size is 0.
  *              Caller-owned.
  * No y may overlap any input or another problem's y.  Ordered on `stream`.
+ * A launch's CTAs may wait, within the wait limit (bd_set_wait_limit_ns), for
+ * other CTAs of the same launch that share a row block; the launch is sized
+ * to be resident on the GPU at once, so a launch kept from becoming resident
+ * for longer than the limit (long-running kernels on other streams holding
+ * the SMs) reports BD_ERR_DEVICE_TIMEOUT instead of completing.
  * Errors: the first failing problem's bd_linear code (nothing launched),
  *         BD_ERR_INVALID_ARG (n out of range, reserved != 0),
  *         BD_ERR_WORKSPACE (missing, misaligned or too small), BD_ERR_CUDA;
