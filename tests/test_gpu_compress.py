@@ -195,3 +195,18 @@ def test_batched_compression_workspace_errors():
         bd.bd_compress_batch(descs, torch.empty(need - 256, dtype=torch.uint8, device="cuda"))
     assert e.value.status == bd.BD_ERR_WORKSPACE
     assert bd.bd_compress_batch_workspace_size((bd.CompressDesc * 0)()) == 0
+
+
+def test_batched_compression_of_the_llama3_8b_stack_shapes():
+    """One layer of the Llama-3-8B-shape stack (q, k, v, o, gate, up, down) in one batched call."""
+    c = workloads.LLAMA3_8B_STACK
+    mats = []
+    for i, (_, n_out, n_in) in enumerate(c["matrices"]):
+        w_base, w_ft = synth.matrix_pair(n_out, n_in, c["sigma"], c["b"], workloads.matrix_seed(c["seed"], i), "cuda")
+        mats.append((w_base, w_ft, c["mode"]))
+    outs = gpu_compress_batch(mats)
+    for (w_base, w_ft, mode), (bits, alpha) in zip(mats, outs):
+        wb, wf = synth.as_u16(w_base), synth.as_u16(w_ft)
+        assert np.array_equal(bits.cpu().numpy(), oracle.sign_bits(wb, wf))
+        a64 = oracle.alpha(wb, wf, mode)
+        assert abs(float(alpha[0]) - a64[0]) / abs(a64[0]) <= ALPHA_REL

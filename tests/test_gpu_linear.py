@@ -135,6 +135,22 @@ def test_llama70b_prefill_full_size(idx):
     torch.cuda.empty_cache()
 
 
+# the distinct matrix shapes of the Llama-3-8B-shape stack (k and v share one, gate and up another)
+STACK_SHAPES = sorted({(n, a, b) for (n, a, b) in workloads.LLAMA3_8B_STACK["matrices"] if n in ("q", "k", "gate", "down")})
+
+
+@pytest.mark.parametrize("idx", range(len(STACK_SHAPES)))
+def test_llama3_8b_stack_shapes_full_size(idx):
+    c = workloads.LLAMA3_8B_STACK
+    name, n_out, n_in = STACK_SHAPES[idx]
+    case = LinearCase(n_out, n_in, 1, c["sigma"], c["b"], c["mode"], workloads.matrix_seed(c["seed"], idx))
+    for m in c["ms"]:
+        case.set_m(m, seed=3000 + m)
+        sampled_check(case, AUTO, 1500, f"{name} m={m}")
+    del case
+    torch.cuda.empty_cache()
+
+
 def test_both_kernels_agree_with_oracle_at_the_dispatch_boundary():
     for m in (63, 64, 65):
         case = LinearCase(512, 2048, m, seed=m)
