@@ -148,6 +148,29 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// ---- thread-block clusters ---------------------------------------------------------
+// Split cluster barrier: arrive (release) now, wait (acquire) later; every thread of
+// every CTA of the cluster takes part, once each.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of `local_addr` (this CTA's shared memory) in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t local_addr, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+// Asynchronous 4-byte store into another CTA's shared memory; its bytes count on that
+// CTA's mbarrier (complete_tx).
+__device__ __forceinline__ void st_async_remote_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
+
 // Programmatic dependent launch: let the next kernel on the stream start its
 // prologue, then wait until every kernel this one depends on has completed
 // and its writes are visible.  Both are no-ops without the launch attribute.

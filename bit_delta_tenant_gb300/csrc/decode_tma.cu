@@ -24,8 +24,12 @@
 // columns are 16t..16t+15 of the half, and the k-slots of the four MMAs per
 // half map to those columns in order, identically for the activations.  A
 // cluster of C CTAs splits K; partials are added across the two halves in
-// shared memory and across the cluster through distributed shared memory, in
-// a fixed order.
+// shared memory, and across the cluster by push: rank c owns a share of the
+// block's rows, every other rank stores its partial of those rows straight
+// into c's shared-memory inbox with st.async (the bytes counted on c's
+// mbarrier), and c adds the ranks' partials in rank order (a fixed order) and
+// writes y.  No rank reads another's shared memory, so none waits for its
+// peers before it exits.
 // Launches allow programmatic dependent launch: the next kernel on the stream
 // may start its prologue while this one drains.  Every global read comes after
 // griddepcontrol.wait, so data written by the previous kernel is seen -- except,
@@ -52,8 +56,11 @@ constexpr int kMaxSmem = 227 * 1024;        // opt-in dynamic shared memory per 
 constexpr size_t kSmemPerSm = 228 * 1024;   // shared memory of one SM (1 KB of it reserved per CTA)
 
 __host__ __device__ constexpr uint32_t red_bytes(int rg, int nt) { return 8u * nt * 16u * rg * 4u; }
+// Inbox of the cluster reduction: [sender rank][token][owned row], at most (rows + 8) x MP floats.
+__host__ __device__ constexpr uint32_t inbox_bytes(int rg, int nt) { return (16u * rg + 8u) * 8u * nt * 4u; }
 inline size_t smem_bytes(int rg, int nt, int stages) {
-    return 1024 + static_cast<size_t>(stages) * stage_layout(rg, nt).stage + red_bytes(rg, nt) + 2 * stages * 8 + 16;
+    return 1024 + static_cast<size_t>(stages) * stage_layout(rg, nt).stage + red_bytes(rg, nt) + inbox_bytes(rg, nt) +
+           (2 * stages + 1) * 8 + 16;
 }
 
 struct TmaDecodeArgs {
@@ -88,9 +95,11 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     constexpr StageLayout L = stage_layout(RG, NT);
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *red = reinterpret_cast<float *>(smem + kStages * L.stage);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * L.stage + red_bytes(rg_n, NT));
+    float *inbox = red + red_bytes(rg_n, NT) / 4;
+    uint64_t *full = reinterpret_cast<uint64_t *>(inbox + inbox_bytes(rg_n, NT) / 4);
     uint64_t *empty = full + kStages;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kStages);
+    uint64_t *inbox_bar = empty + kStages;  // completes when every peer's rows of this rank have landed
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(inbox_bar + 1);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
@@ -103,15 +112,25 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     const int lane = threadIdx.x & 31;
     const bool is_producer = warp == n_cons;
 
+    // Cluster reduction by push: rank c owns rows [c*share, c*share + owned(c)) of the block;
+    // each peer stores its partial of those rows into c's inbox (st.async, counted in bytes
+    // on c's inbox barrier), and c adds the ranks' partials in rank order.
+    const int share = (rows + a.cluster - 1) / a.cluster;
+    const int m_here = static_cast<int>(a.m < MP ? a.m : MP);
+    auto owned = [&](int q) { return max(0, min(share, rows - q * share)); };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], n_cons);
         }
+        mbar_init(inbox_bar, 1);
+        mbar_arrive_expect_tx(inbox_bar,
+                              static_cast<uint32_t>((a.cluster - 1) * owned(rank) * m_here) * sizeof(float));
         *abort_flag = 0;
         mbar_fence_init();
     }
     __syncthreads();
+    cluster_arrive_release();  // peers push into this CTA only after they have seen its barriers initialised
     pdl_trigger();
     const int n_pre = a.prefetch_weights ? min(n_steps, kStages) : 0;
     if (is_producer && lane == 0 && n_pre > 0) {
@@ -203,24 +222,41 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
         if (kh == 1) dstage::halves_store<NT>(red, rows, r0, t, part);
         asm volatile("bar.sync 1, %0;" ::"n"(32 * n_cons) : "memory");  // consumer warps only
         if (kh == 0) dstage::halves_add<NT>(red, rows, r0, t, part);
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * n_cons) : "memory");  // red complete
     }
-    cluster.sync();
+    __syncwarp();
+    cluster_wait_acquire();  // every peer's inbox barrier is initialised
+    if (is_producer) return;
 
-    // ---- rank c sums rows [c*share, (c+1)*share) of the block over the cluster ----
-    const int share = (rows + a.cluster - 1) / a.cluster;
-    const int m_here = static_cast<int>(a.m < MP ? a.m : MP);
-    for (int i = threadIdx.x; i < share * m_here; i += blockDim.x) {
-        const int tok = i / share;
-        const int lr = rank * share + (i - tok * share);
+    // ---- push the rows other ranks own (this rank's partial; garbage after a timeout, but always sent) ----
+    const int ctid = threadIdx.x;  // consumer threads: 0 .. 32 * n_cons - 1
+    const uint32_t inbox_addr = smem_u32(inbox), bar_addr = smem_u32(inbox_bar);
+    for (int e = ctid; e < m_here * rows; e += 32 * n_cons) {
+        const int tok = e / rows, lr = e - tok * rows;
+        const int q = lr / share;
+        if (q == rank) continue;
+        const uint32_t idx = static_cast<uint32_t>((rank * MP + tok) * share + (lr - q * share));
+        st_async_remote_f32(mapa_rank(inbox_addr + idx * 4u, q), red[tok * rows + lr], mapa_rank(bar_addr, q));
+    }
+    // ---- add this rank's rows over the cluster in rank order and write y ----
+    const int mine = owned(rank);
+    if (mine == 0) return;
+    if (!mbar_wait(inbox_bar, 0, a.wait_ns + kDrainLimitNs, nullptr)) {  // peers always push: bounded drain
+        if (ctid == 0) flag_status(a.status, kDevTimeout);
+        return;
+    }
+    for (int e = ctid; e < m_here * mine; e += 32 * n_cons) {
+        const int tok = e / mine, lrl = e - tok * mine;
+        const int lr = rank * share + lrl;
         const int64_t row = static_cast<int64_t>(row0) + lr;
-        if (lr < rows && row < a.n_out) {
-            float s = 0.0f;
-            for (int q = 0; q < a.cluster; ++q) s += cluster.map_shared_rank(red, q)[tok * rows + lr];
+        float s = 0.0f;
+        for (int q = 0; q < a.cluster; ++q)
+            s += q == rank ? red[tok * rows + lr] : inbox[(q * MP + tok) * share + lrl];
+        if (row < a.n_out) {
             __nv_bfloat16 h = __float2bfloat16_rn(s);
             a.y[static_cast<int64_t>(tok) * a.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
         }
     }
-    cluster.sync();
 }
 
 struct TmaPlan {
