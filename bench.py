@@ -215,22 +215,25 @@ def compress_phase(bd, mats, mode, dev):
 # and inside the linear graph no kernel writes weights.
 WEIGHT_PREFETCH = True
 
-# How a layer's fused linears are issued: "layer" passes the projections that share
-# their input in a real layer -- q, k, v and gate, up -- to one bd_linear_batch call
-# each (o and down alone, through the same entry); "none" calls bd_linear per matrix.
-LINEAR_BATCH = "layer"
+# How a layer's fused linears are issued: "layer" passes the projections that share their
+# input in a real layer -- q, k, v and gate, up -- to one bd_linear_batch call each; "qkv"
+# batches q, k, v only; "none" calls bd_linear per matrix (a call of one problem runs as
+# bd_linear either way).  "auto" takes the workload's own choice, measured on GB300: the
+# Llama-7B layer batches q/k/v only (its 11008-row gate and up run faster alone, on the
+# cluster-split kernel's balanced plan), the Llama-3-8B stack batches both groups.
+LINEAR_BATCH = "auto"
+FUSED_GROUPS = ({"q", "k", "v"}, {"gate", "up"})
 # Compressions issued through bd_compress_batch (up to 8 matrices per call); --compress-batch 0
 # issues one bd_compress per matrix.
 COMPRESS_BATCH = True
-FUSED_GROUPS = ({"q", "k", "v"}, {"gate", "up"})
 
 
-def layer_groups(names):
+def layer_groups(names, fused=FUSED_GROUPS):
     """Consecutive indices of `names` ("L<l>.<matrix>") that one batched call takes."""
     groups, i = [], 0
     while i < len(names):
         layer, base = names[i].split(".", 1)
-        grp = next((g for g in FUSED_GROUPS if base in g), None)
+        grp = next((g for g in fused if base in g), None)
         j = i + 1
         while grp is not None and j < len(names) and names[j].split(".", 1)[0] == layer \
                 and names[j].split(".", 1)[1] in grp:
@@ -273,7 +276,7 @@ class LayerWorkload(Workload):
     Used for the Llama-7B layer at decode sizes (the default), the 70B-shape
     prefill linears and the Llama-3-8B-shape stack (decode or prefill)."""
 
-    def __init__(self, bd, dev, cfg, ms, unit, name, layers=1, private_io=True):
+    def __init__(self, bd, dev, cfg, ms, unit, name, layers=1, private_io=True, batch="layer"):
         self.cfg, self.metric_unit = cfg, unit
         mode = cfg["mode"]
         shapes = [(f"L{l}.{n}", a, b) for l in range(layers) for (n, a, b) in cfg["matrices"]]
@@ -283,8 +286,10 @@ class LayerWorkload(Workload):
         self.comp, self.packed = compress_phase(bd, self.mats, mode, dev)
         self.xs, self.ys = {}, {}
         calls, nbytes, flops, launches = [], 0.0, 0.0, 0
-        groups = layer_groups([n for n, _, _ in shapes]) if LINEAR_BATCH == "layer" else \
-            [[i] for i in range(len(shapes))]
+        names = [n for n, _, _ in shapes]
+        self.batch = batch if LINEAR_BATCH == "auto" else LINEAR_BATCH
+        groups = layer_groups(names) if self.batch == "layer" else \
+            layer_groups(names, FUSED_GROUPS[:1]) if self.batch == "qkv" else [[i] for i in range(len(shapes))]
         self.batch_ws = None
         self.linear_plan = []  # (matrices the call needs, call) for the pipelined end-to-end step
         for m in ms:
@@ -304,7 +309,7 @@ class LayerWorkload(Workload):
                     probs.append((self.xs[xk], self.mats[i][0], bits, alpha, mode, self.ys[yk]))
                     nbytes += decode_bytes(m, n_out, n_in, mode)
                     flops += 2.0 * m * n_out * n_in
-                if LINEAR_BATCH == "layer":
+                if self.batch in ("layer", "qkv"):
                     descs = bd.linear_descs(probs)
                     need = bd.bd_linear_batch_workspace_size(descs)
                     if need > 0 and (self.batch_ws is None or self.batch_ws.numel() < need):
@@ -334,7 +339,7 @@ class LayerWorkload(Workload):
         self.config = {"workload": name, "matrices": sorted({f"{a}x{b}" for _, a, b in shapes}),
                        "matrix_count": len(shapes), "tokens": list(ms),
                        "alpha": "per-row" if mode == 1 else "scalar", "dtype_in": "bf16 weights/activations",
-                       "weight_prefetch": WEIGHT_PREFETCH, "linear_batch": LINEAR_BATCH,
+                       "weight_prefetch": WEIGHT_PREFETCH, "linear_batch": self.batch,
                        "compress_batch": COMPRESS_BATCH,
                        "l2": "inputs larger than L2 (consecutive uses of a matrix separated by >250 MB of traffic)"}
 
@@ -519,7 +524,8 @@ class GroupedStackWorkload(Workload):
 
 WORKLOADS = {
     "llama7b_layer_decode": lambda bd, dev: LayerWorkload(
-        bd, dev, workloads.LLAMA7B_LAYER, workloads.LLAMA7B_LAYER["ms"], "GB/s", "llama7b_layer_decode"),
+        bd, dev, workloads.LLAMA7B_LAYER, workloads.LLAMA7B_LAYER["ms"], "GB/s", "llama7b_layer_decode",
+        batch="qkv"),
     "llama70b_linears_prefill": lambda bd, dev: LayerWorkload(
         bd, dev, workloads.LLAMA70B_PREFILL, workloads.LLAMA70B_PREFILL["ms"], "TFLOP/s", "llama70b_linears_prefill",
         private_io=False),
@@ -1051,8 +1057,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--weight-prefetch", type=int, choices=[0, 1], default=1,
                     help="capture the device-resident fused linears with bd_set_weight_prefetch(1)")
-    ap.add_argument("--linear-batch", choices=["none", "layer"], default="layer",
-                    help="layer: q/k/v and gate/up of a layer in one bd_linear_batch call each")
+    ap.add_argument("--linear-batch", choices=["auto", "none", "qkv", "layer"], default="auto",
+                    help="layer: q/k/v and gate/up of a layer in one bd_linear_batch call each; qkv: q/k/v only; "
+                         "auto: the workload's own choice")
     ap.add_argument("--compress-batch", type=int, choices=[0, 1], default=1,
                     help="compress through bd_compress_batch (8 matrices per call) or one bd_compress each")
     ap.add_argument("--kernel-case", default=None,
