@@ -642,7 +642,7 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-KERNEL_SOURCES = {"hbm": ("decode_tma.cu", "decode_batch.cu", "decode_stage.cuh"), "tensor": ("prefill.cu",)}
+KERNEL_SOURCES = {"hbm": ("decode_tma.cu", "decode_batch.cu", "decode_stage.cuh", "api.cu"), "tensor": ("prefill.cu",)}
 
 
 def lookup_traffic(workload: str, phase):

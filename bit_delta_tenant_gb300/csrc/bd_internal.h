@@ -119,6 +119,11 @@ struct BatchPlan {
 bool decode_batch_supported(int64_t m, int64_t n_out, int64_t n_in, const void *x, const void *w_base,
                             const uint8_t *bits, const void *y);
 BatchPlan plan_decode_batch(const BatchItem *items, int n, const DevCtx &ctx);
+// The same list on the cluster-split kernel (decode_tma.cu): one launch, every linear's
+// 64-row blocks split over one cluster size; no workspace.
+bool decode_tma_multi_supported(const BatchItem *items, int n);
+bool decode_tma_multi_one_wave(const BatchItem *items, int n, const DevCtx &ctx);  // its CTAs fit at once
+cudaError_t launch_decode_tma_multi(const BatchItem *items, int n, const DevCtx &ctx, cudaStream_t stream);
 cudaError_t launch_decode_batch(const BatchItem *items, int n, const BatchPlan &plan, void *workspace,
                                 const DevCtx &ctx, cudaStream_t stream);
 

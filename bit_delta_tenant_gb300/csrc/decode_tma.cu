@@ -63,12 +63,26 @@ inline size_t smem_bytes(int rg, int nt, int stages) {
            (2 * stages + 1) * 8 + 16;
 }
 
-struct TmaDecodeArgs {
+// One launch streams up to kTmaMaxLinears independent linears (bd_linear_batch);
+// bd_linear is a list of one.  Linear p owns CTAs [first_cta, first_cta + blocks *
+// cluster), so no cluster spans two linears.
+constexpr int kTmaMaxLinears = 8;
+struct TmaLinear {
     const float *alpha;
     uint16_t *y;
     int64_t m, n_out, n_in;
-    int64_t ks;
+    int64_t ks;           // K columns per cluster rank
     int32_t mode;
+    int32_t first_cta;
+};
+struct TmaMaps {
+    CUtensorMap w[kTmaMaxLinears];
+    CUtensorMap b[kTmaMaxLinears];
+    CUtensorMap x[kTmaMaxLinears];
+};
+struct TmaDecodeArgs {
+    TmaLinear lin[kTmaMaxLinears];
+    int32_t n_lin;
     int32_t cluster;
     int32_t rg;                // row groups of 16 rows per CTA
     int32_t stages;            // ring depth
@@ -84,8 +98,7 @@ __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *stat
 
 template <int NT, int RG>
 __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
-    decode_tma_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
-                      const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ TmaDecodeArgs a) {
+    decode_tma_kernel(const __grid_constant__ TmaMaps maps, const __grid_constant__ TmaDecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int MP = 8 * NT;
     constexpr int rg_n = RG;
@@ -103,10 +116,14 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
-    const int64_t row_block = blockIdx.x / a.cluster;
+    int lp = 0;  // this CTA's linear
+    while (lp + 1 < a.n_lin && a.lin[lp + 1].first_cta <= static_cast<int>(blockIdx.x)) ++lp;
+    const TmaLinear &P = a.lin[lp];
+    const CUtensorMap *tm_w = &maps.w[lp], *tm_b = &maps.b[lp], *tm_x = &maps.x[lp];
+    const int64_t row_block = (blockIdx.x - P.first_cta) / a.cluster;
     const int row0 = static_cast<int>(row_block * rows);
-    const int64_t k_lo = static_cast<int64_t>(rank) * a.ks;
-    const int64_t k_hi = min(k_lo + a.ks, a.n_in);
+    const int64_t k_lo = static_cast<int64_t>(rank) * P.ks;
+    const int64_t k_hi = min(k_lo + P.ks, P.n_in);
     const int n_steps = k_hi > k_lo ? static_cast<int>((k_hi - k_lo + kStepK - 1) / kStepK) : 0;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -116,7 +133,7 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     // each peer stores its partial of those rows into c's inbox (st.async, counted in bytes
     // on c's inbox barrier), and c adds the ranks' partials in rank order.
     const int share = (rows + a.cluster - 1) / a.cluster;
-    const int m_here = static_cast<int>(a.m < MP ? a.m : MP);
+    const int m_here = static_cast<int>(P.m < MP ? P.m : MP);
     auto owned = [&](int q) { return max(0, min(share, rows - q * share)); };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -136,15 +153,15 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     if (is_producer && lane == 0 && n_pre > 0) {
         // Weights are not written by the preceding kernel (the caller's
         // promise): start streaming them before that kernel completes.
-        tma_prefetch_desc(&tm_w);
-        tma_prefetch_desc(&tm_b);
+        tma_prefetch_desc(tm_w);
+        tma_prefetch_desc(tm_b);
         for (int i = 0; i < n_pre; ++i) {
             const int kc = static_cast<int>(k_lo) + i * kStepK;
             uint8_t *st = smem + i * L.stage;
             mbar_arrive_expect_tx(&full[i], L.tx);
-            tma_load_2d(st, &tm_w, &full[i], kc, row0);
-            tma_load_2d(st + L.w_box, &tm_w, &full[i], kc + 64, row0);
-            tma_load_2d(st + L.bits_off, &tm_b, &full[i], kc / 8, row0);
+            tma_load_2d(st, tm_w, &full[i], kc, row0);
+            tma_load_2d(st + L.w_box, tm_w, &full[i], kc + 64, row0);
+            tma_load_2d(st + L.bits_off, tm_b, &full[i], kc / 8, row0);
         }
     }
     pdl_wait();
@@ -163,14 +180,14 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     if (is_producer) {
         // ---- producer ----
         if (lane == 0) {
-            tma_prefetch_desc(&tm_w);
-            tma_prefetch_desc(&tm_b);
-            tma_prefetch_desc(&tm_x);
+            tma_prefetch_desc(tm_w);
+            tma_prefetch_desc(tm_b);
+            tma_prefetch_desc(tm_x);
             for (int i = 0; i < n_pre; ++i) {  // the activations of the prefetched stages
                 const int kc = static_cast<int>(k_lo) + i * kStepK;
                 uint8_t *st = smem + i * L.stage;
-                tma_load_2d(st + L.x_off, &tm_x, &full[i], kc, 0);
-                tma_load_2d(st + L.x_off + L.x_box, &tm_x, &full[i], kc + 64, 0);
+                tma_load_2d(st + L.x_off, tm_x, &full[i], kc, 0);
+                tma_load_2d(st + L.x_off + L.x_box, tm_x, &full[i], kc + 64, 0);
             }
             int issued = n_pre;
             int s = n_pre % kStages;  // slot and phase advance incrementally (the ring depth is a launch value)
@@ -183,17 +200,17 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
                 const int kc = static_cast<int>(k_lo) + i * kStepK;
                 uint8_t *st = smem + s * L.stage;
                 mbar_arrive_expect_tx(&full[s], L.tx);
-                tma_load_2d(st, &tm_w, &full[s], kc, row0);
-                tma_load_2d(st + L.w_box, &tm_w, &full[s], kc + 64, row0);
-                tma_load_2d(st + L.bits_off, &tm_b, &full[s], kc / 8, row0);
-                tma_load_2d(st + L.x_off, &tm_x, &full[s], kc, 0);
-                tma_load_2d(st + L.x_off + L.x_box, &tm_x, &full[s], kc + 64, 0);
+                tma_load_2d(st, tm_w, &full[s], kc, row0);
+                tma_load_2d(st + L.w_box, tm_w, &full[s], kc + 64, row0);
+                tma_load_2d(st + L.bits_off, tm_b, &full[s], kc / 8, row0);
+                tma_load_2d(st + L.x_off, tm_x, &full[s], kc, 0);
+                tma_load_2d(st + L.x_off + L.x_box, tm_x, &full[s], kc + 64, 0);
                 issued = i + 1;
             }
-            if (*abort_flag) {
-                for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-                    mbar_wait(&full[i % kStages], (i / kStages) & 1, kDrainLimitNs, nullptr);
-            }
+            // Every copy issued has landed before the CTA can exit, also when the consumers gave up
+            // after this loop ended (in a normal run these phases are complete and the waits return).
+            for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+                mbar_wait(&full[i % kStages], (i / kStages) & 1, kDrainLimitNs, nullptr);
         }
     } else {
         // ---- consumers ----
@@ -214,9 +231,9 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
 
         // ---- fold alpha, add the two halves ----
         const int64_t grow0 = static_cast<int64_t>(row0) + r0;
-        const bool v0 = grow0 < a.n_out, v1 = grow0 + 8 < a.n_out;
-        const float al0 = v0 ? (a.mode ? a.alpha[grow0] : a.alpha[0]) : 0.0f;
-        const float al1 = v1 ? (a.mode ? a.alpha[grow0 + 8] : a.alpha[0]) : 0.0f;
+        const bool v0 = grow0 < P.n_out, v1 = grow0 + 8 < P.n_out;
+        const float al0 = v0 ? (P.mode ? P.alpha[grow0] : P.alpha[0]) : 0.0f;
+        const float al1 = v1 ? (P.mode ? P.alpha[grow0 + 8] : P.alpha[0]) : 0.0f;
         float part[NT][4];
         dstage::fold_alpha<NT>(accb, accs, al0, al1, part);
         if (kh == 1) dstage::halves_store<NT>(red, rows, r0, t, part);
@@ -252,9 +269,9 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
         float s = 0.0f;
         for (int q = 0; q < a.cluster; ++q)
             s += q == rank ? red[tok * rows + lr] : inbox[(q * MP + tok) * share + lrl];
-        if (row < a.n_out) {
+        if (row < P.n_out) {
             __nv_bfloat16 h = __float2bfloat16_rn(s);
-            a.y[static_cast<int64_t>(tok) * a.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
+            P.y[static_cast<int64_t>(tok) * P.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
         }
     }
 }
@@ -361,12 +378,12 @@ bool make_tma_plan(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx, Tm
 }
 
 template <int NT, int RG>
-cudaError_t launch_plan(const CUtensorMap &tw, const CUtensorMap &tb, const CUtensorMap &tx, const TmaDecodeArgs &a,
-                        const TmaPlan &p, const DevCtx &ctx, cudaStream_t stream) {
+cudaError_t launch_plan(const TmaMaps &maps, const TmaDecodeArgs &a, int64_t ctas, const TmaPlan &p,
+                        const DevCtx &ctx, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attr<NT, RG>(ctx.device);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.row_blocks * p.cluster), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(32 * (2 * RG + 1)), 1, 1);
     cfg.dynamicSmemBytes = smem_bytes(RG, NT, p.stages);
     cfg.stream = stream;
@@ -379,18 +396,52 @@ cudaError_t launch_plan(const CUtensorMap &tw, const CUtensorMap &tb, const CUte
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_tma_kernel<NT, RG>, tw, tb, tx, a);
+    return cudaLaunchKernelEx(&cfg, decode_tma_kernel<NT, RG>, maps, a);
 }
 
-cudaError_t launch_any(const CUtensorMap &tw, const CUtensorMap &tb, const CUtensorMap &tx, const TmaDecodeArgs &a,
-                       const TmaPlan &p, const DevCtx &ctx, cudaStream_t stream) {
+cudaError_t launch_any(const TmaMaps &maps, const TmaDecodeArgs &a, int64_t ctas, const TmaPlan &p,
+                       const DevCtx &ctx, cudaStream_t stream) {
 #define BD_DECODE_CASE(NT_, RG_) \
-    if (p.nt == NT_ && p.rg == RG_) return launch_plan<NT_, RG_>(tw, tb, tx, a, p, ctx, stream);
+    if (p.nt == NT_ && p.rg == RG_) return launch_plan<NT_, RG_>(maps, a, ctas, p, ctx, stream);
     BD_DECODE_CASE(1, 4) BD_DECODE_CASE(1, 5) BD_DECODE_CASE(1, 6) BD_DECODE_CASE(1, 7) BD_DECODE_CASE(1, 8)
     BD_DECODE_CASE(2, 4) BD_DECODE_CASE(2, 5) BD_DECODE_CASE(2, 6) BD_DECODE_CASE(2, 7) BD_DECODE_CASE(2, 8)
     BD_DECODE_CASE(4, 4) BD_DECODE_CASE(4, 7) BD_DECODE_CASE(8, 4)
 #undef BD_DECODE_CASE
     return cudaErrorNotSupported;
+}
+
+// Tensor maps and entry of linear i of a launch with `rows`-row blocks and token tiles of MP rows.
+bool fill_linear(TmaMaps &maps, TmaDecodeArgs &a, int i, const void *x, int64_t m, const void *w_base,
+                 const uint8_t *bits, const float *alpha, int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y,
+                 uint32_t rows, int mp, int64_t ks, int64_t first_cta) {
+    if (!encode_tensor_map_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, 64, rows,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&maps.b[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, bits, n_in / 8, n_out, n_in / 8, 16, rows,
+                              CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tensor_map_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, m, n_in * 2, 64,
+                              static_cast<uint32_t>(mp), CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    if (first_cta > 0x7FFFFFFFLL) return false;
+    TmaLinear &l = a.lin[i];
+    l.alpha = alpha;
+    l.y = static_cast<uint16_t *>(y);
+    l.m = m;
+    l.n_out = n_out;
+    l.n_in = n_in;
+    l.ks = ks;
+    l.mode = alpha_mode;
+    l.first_cta = static_cast<int32_t>(first_cta);
+    return true;
+}
+
+void fill_common(TmaDecodeArgs &a, const TmaPlan &p, int n_lin, const DevCtx &ctx) {
+    a.n_lin = n_lin;
+    a.cluster = p.cluster;
+    a.rg = p.rg;
+    a.stages = p.stages;
+    a.prefetch_weights = ctx.weight_prefetch ? 1 : 0;
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
 }
 
 }  // namespace
@@ -409,34 +460,82 @@ cudaError_t launch_decode_tma(const void *x, int64_t m, const void *w_base, cons
                               cudaStream_t stream) {
     TmaPlan p;
     if (!make_tma_plan(m, n_out, n_in, ctx, p)) return cudaErrorNotSupported;
-    const uint32_t rows = static_cast<uint32_t>(16 * p.rg);
-    CUtensorMap tw, tb;
-    if (!encode_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, 64, rows,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
+    TmaMaps maps;
+    TmaDecodeArgs a{};
+    if (!fill_linear(maps, a, 0, x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y,
+                     static_cast<uint32_t>(16 * p.rg), 8 * p.nt, p.ks, 0))
         return cudaErrorInvalidValue;
-    if (!encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bits, n_in / 8, n_out, n_in / 8, 16, rows,
-                              CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    const int mp = 8 * p.nt;
-    CUtensorMap tx;
-    if (!encode_tensor_map_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, m, n_in * 2, 64,
-                              static_cast<uint32_t>(mp), CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    TmaDecodeArgs a;
-    a.alpha = alpha;
-    a.y = static_cast<uint16_t *>(y);
-    a.m = m;
-    a.n_out = n_out;
-    a.n_in = n_in;
-    a.ks = p.ks;
-    a.mode = alpha_mode;
-    a.cluster = p.cluster;
-    a.rg = p.rg;
-    a.stages = p.stages;
-    a.prefetch_weights = ctx.weight_prefetch ? 1 : 0;
-    a.status = ctx.status;
-    a.wait_ns = ctx.wait_ns;
-    return launch_any(tw, tb, tx, a, p, ctx, stream);
+    fill_common(a, p, 1, ctx);
+    return launch_any(maps, a, p.row_blocks * p.cluster, p, ctx, stream);
+}
+
+bool decode_tma_multi_supported(const BatchItem *items, int n) {
+    if (n < 1 || n > kTmaMaxLinears) return false;
+    for (int i = 0; i < n; ++i)
+        if (items[i].m < 1 || items[i].m > 16 || items[i].n_in % kStepK != 0 ||
+            items[i].n_in >= (int64_t(1) << 31) - kStepK || (reinterpret_cast<uintptr_t>(items[i].w_base) & 15) ||
+            (reinterpret_cast<uintptr_t>(items[i].bits) & 15))
+            return false;
+    return true;
+}
+
+// Several linears (m <= 16) in one launch of the cluster-split kernel: 64-row CTAs, two per SM,
+// one K split C for all of them from their blocks together, the same rule as for one linear
+// (C = ceil(1.5 * SMs / blocks) while the blocks leave SMs idle; BD_DECODE_CLUSTER overrides).
+struct MultiShape {
+    int64_t mmax, blocks, min_steps;
+    int cluster;
+};
+MultiShape multi_shape(const BatchItem *items, int n, const DevCtx &ctx) {
+    MultiShape m{0, 0, -1, 1};
+    for (int i = 0; i < n; ++i) {
+        m.mmax = items[i].m > m.mmax ? items[i].m : m.mmax;
+        m.blocks += (items[i].n_out + 63) / 64;
+        const int64_t st = items[i].n_in / kStepK;
+        m.min_steps = m.min_steps < 0 || st < m.min_steps ? st : m.min_steps;
+    }
+    int c = m.blocks >= ctx.num_sms
+                ? 1
+                : static_cast<int>((3 * static_cast<int64_t>(ctx.num_sms) / 2 + m.blocks - 1) / m.blocks);
+    c = env_int("BD_DECODE_CLUSTER", c);
+    if (c > 8) c = 8;
+    if (c > m.min_steps) c = static_cast<int>(m.min_steps);
+    m.cluster = c < 1 ? 1 : c;
+    return m;
+}
+
+bool decode_tma_multi_one_wave(const BatchItem *items, int n, const DevCtx &ctx) {
+    if (!decode_tma_multi_supported(items, n)) return false;
+    const MultiShape m = multi_shape(items, n, ctx);
+    return m.blocks * m.cluster <= 2 * static_cast<int64_t>(ctx.num_sms);  // two 64-row CTAs per SM
+}
+
+cudaError_t launch_decode_tma_multi(const BatchItem *items, int n, const DevCtx &ctx, cudaStream_t stream) {
+    if (!decode_tma_multi_supported(items, n)) return cudaErrorNotSupported;
+    const MultiShape ms = multi_shape(items, n, ctx);
+    const int c = ms.cluster;
+    TmaPlan p;
+    p.nt = ms.mmax <= 8 ? 1 : 2;
+    p.rg = 4;
+    p.cluster = c;
+    p.stages = p.nt == 1 ? 5 : 4;
+    TmaMaps maps;
+    TmaDecodeArgs a{};
+    int64_t first = 0;
+    for (int i = 0; i < n; ++i) {
+        const BatchItem &it = items[i];
+        const int64_t steps = it.n_in / kStepK;
+        const int64_t ks = (steps + c - 1) / c * kStepK;
+        if (!fill_linear(maps, a, i, it.x, it.m, it.w_base, it.bits, it.alpha, it.alpha_mode, it.n_out, it.n_in, it.y,
+                         64u, 8 * p.nt, ks, first))
+            return cudaErrorInvalidValue;
+        first += (it.n_out + 63) / 64 * c;
+    }
+    fill_common(a, p, n, ctx);
+    if (std::getenv("BD_DECODE_PLAN_VERBOSE"))
+        std::fprintf(stderr, "decode plan, %d linears, m<=%d: R=4 C=%d CTAs=%lld\n", n, 8 * p.nt, c,
+                     static_cast<long long>(first));
+    return launch_any(maps, a, first, p, ctx, stream);
 }
 
 }  // namespace bd

@@ -200,12 +200,14 @@ int32_t bd_linear(const void *x, int64_t m, const void *w_base,
  * Problems with 1 <= m <= 16, n_in a multiple of 128 and x, w_base, bits
  * and y 16-byte aligned are streamed together: up to
  * BD_LINEAR_BATCH_PER_LAUNCH of them per launch (grouped by m <= 8 and
- * m <= 16), with their work items -- one 128-column K step of one 64-row
- * block -- split evenly over the resident CTAs.  A row block that several
- * CTAs share is summed from fp32 partials in a fixed order, so results are
- * deterministic; they may differ from bd_linear's in the last bits of fp32
- * rounding (another split of K).  Every other problem, and a group that
- * would hold a single problem, runs as bd_linear.
+ * m <= 16).  A launch whose 64-row blocks, times one K split shared by all
+ * its problems, fit on the GPU at once runs them as one streaming launch
+ * with K split over clusters; otherwise their work items -- one 128-column K
+ * step of one 64-row block -- are split evenly over the resident CTAs.
+ * Either way a row block's fp32 partials are summed in a fixed order, so
+ * results are deterministic; they may differ from bd_linear's in the last
+ * bits of fp32 rounding (another split of K).  Every other problem, and a
+ * group that would hold a single problem, runs as bd_linear.
  *
  *   descs      host array [n] of bd_linear_desc (read during the call only;
  *              `reserved` must be 0)

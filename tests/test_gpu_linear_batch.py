@@ -2,9 +2,11 @@
 
 Each problem of a batch must match the oracle's fused linear on the same seeded
 inputs; small problems compare every output, full-size ones sampled outputs.
-The work split (one 128-column K step of one 64-row block per work item, split
-evenly over the CTAs) is exercised with the default grid and with forced grids
-that make row blocks shared by many CTAs or by none."""
+Both kernels a launch can run are exercised, by the library's choice and forced:
+the cluster-split one (64-row CTAs, K split over a cluster, partials pushed to the
+owning CTA) and the evenly split one (one 128-column K step of one 64-row block per
+work item, split evenly over the CTAs), the latter also with forced grids that make
+row blocks shared by many CTAs or by none."""
 import os
 
 import pytest
@@ -51,6 +53,20 @@ def check_all(cases, ys, what):
         assert_y_close(y_host(y), y_ref, mag, f"{what} problem {i} ({c.n_out}x{c.n_in}, m={c.m})")
 
 
+KERNELS = ["auto", "cluster", "streamk"]
+
+
+@pytest.fixture(params=KERNELS)
+def batch_kernel(request, monkeypatch):
+    """The kernel a launch of the batch runs: the library's choice (the cluster-split kernel when
+    its CTAs fit in one wave, else the evenly split one) or either one forced (BD_BATCH_KERNEL)."""
+    if request.param == "auto":
+        monkeypatch.delenv("BD_BATCH_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("BD_BATCH_KERNEL", request.param)
+    return request.param
+
+
 class grid_override:
     """Forces the number of CTAs of the batched kernel (BD_BATCH_GRID)."""
 
@@ -78,7 +94,7 @@ BATCHES = {  # ragged rows (not multiples of 64), several K lengths, both token 
 
 @pytest.mark.parametrize("name", list(BATCHES))
 @pytest.mark.parametrize("mode", [0, 1])
-def test_batches_match_oracle(name, mode):
+def test_batches_match_oracle(name, mode, batch_kernel):
     cases = make_cases(BATCHES[name], seed0=100, mode=mode)
     ys, ws = run_batch(cases)
     check_all(cases, ys, f"{name} mode={mode}")
@@ -86,9 +102,10 @@ def test_batches_match_oracle(name, mode):
 
 
 @pytest.mark.parametrize("grid", [1, 2, 3, 7, 50, 1000, 100000])
-def test_forced_grids(grid):
+def test_forced_grids(grid, monkeypatch):
     """Few CTAs (every block in one CTA's range, several linears per CTA) to far
     more CTAs than items (capped at one item per CTA: every block split K-step by K-step)."""
+    monkeypatch.setenv("BD_BATCH_KERNEL", "streamk")
     cases = make_cases([(200, 1280, 3), (64, 384, 8), (130, 2048, 1)], seed0=300, mode=1)
     with grid_override(grid):
         ys, ws = run_batch(cases)
@@ -107,7 +124,7 @@ def test_single_linear_launch(shape, monkeypatch):
     assert_reusable(cases, ys, ws, f"single {shape}")
 
 
-def test_deterministic_and_equal_across_repeats():
+def test_deterministic_and_equal_across_repeats(batch_kernel):
     cases = make_cases([(512, 4096, 16), (512, 4096, 16), (1000, 2048, 5)], seed0=400)
     ys1, ws = run_batch(cases)
     ys2, _ = run_batch(cases, workspace=ws)
@@ -117,7 +134,7 @@ def test_deterministic_and_equal_across_repeats():
     check_all(cases, ys1, "repeat")
 
 
-def test_more_problems_than_one_launch_and_problems_that_run_alone():
+def test_more_problems_than_one_launch_and_problems_that_run_alone(batch_kernel):
     """11 problems: two launches of the batched kernel plus problems it does not take
     (m > 16: tensor-core kernel; n_in not a multiple of 128: register-fed kernel; m = 0)."""
     shapes = [(128, 256, 1 + i % 8) for i in range(9)] + [(200, 512, 40), (96, 520, 3), (64, 256, 0)]
@@ -134,7 +151,7 @@ def test_more_problems_than_one_launch_and_problems_that_run_alone():
 
 
 @pytest.mark.parametrize("m", [1, 16])
-def test_llama7b_layer_batches_full_size(m):
+def test_llama7b_layer_batches_full_size(m, batch_kernel):
     """q, k, v (4096 x 4096) in one batch and gate, up (11008 x 4096) in another, sampled outputs."""
     c = workloads.LLAMA7B_LAYER
     for group in (("q", "k", "v"), ("gate", "up")):
@@ -153,7 +170,7 @@ def test_llama7b_layer_batches_full_size(m):
 
 
 @pytest.mark.parametrize("m", [1, 9])
-def test_llama3_8b_qkv_batch_full_size_per_row_alpha(m):
+def test_llama3_8b_qkv_batch_full_size_per_row_alpha(m, batch_kernel):
     """q (4096 x 4096) with k and v (1024 x 4096) in one batch, per-row alpha, sampled outputs."""
     shapes = [(4096, 4096), (1024, 4096), (1024, 4096)]
     cases = [LinearCase(n_out, n_in, m, 0.02, 1e-3, 1, seed=750 + i) for i, (n_out, n_in) in enumerate(shapes)]
@@ -168,7 +185,7 @@ def test_llama3_8b_qkv_batch_full_size_per_row_alpha(m):
     assert_reusable(cases, ys, ws, f"qkv m={m}")
 
 
-def test_in_a_graph_with_weight_prefetch_and_a_dependent_batch():
+def test_in_a_graph_with_weight_prefetch_and_a_dependent_batch(batch_kernel):
     """Two batches captured in a graph with weight prefetch on; the second batch
     reads the first one's output as its activations (a read-after-write that a
     premature activation load would miss)."""
@@ -199,7 +216,7 @@ def test_in_a_graph_with_weight_prefetch_and_a_dependent_batch():
     assert_y_close(y_host(yb), y_ref, mag, "graph batch 2 (dependent)")
 
 
-def test_wait_limit_zero_reports_timeout_and_context_survives():
+def test_wait_limit_zero_reports_timeout_and_context_survives(batch_kernel):
     """A zero wait limit makes the batched kernel give up at its first unsatisfied
     wait; it records a timeout, drains its copies and returns.  After zeroing the
     workspace again a normal call is correct."""
