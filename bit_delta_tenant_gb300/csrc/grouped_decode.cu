@@ -17,11 +17,13 @@
 //
 // CTA: 16 warps, each also issuing part of the TMA; 64 W rows.  A ring stage is a
 // 128-column K step: two 64x64 W boxes, two (tokens x 64) activation boxes
-// (128-byte swizzle) and one 64x16-byte packed-bit box per variant.  Consumer
-// warp w owns row group w%4 and every fourth token tile (w/4) over both K
-// halves, processing its sign tiles in interleaved pairs; lane (g, t) reads 16-byte chunks 2t, 2t+1
-// of its rows and of the activation rows, so the MMA k-slots map to columns
-// 16t..16t+15 of the half.  A cluster of C CTAs splits K; each token's base
+// (128-byte swizzle) and one 64x16-byte packed-bit box per variant.  For the
+// base product warp w owns row group w%4 and every fourth token tile (w/4);
+// for the sign products it owns sign tiles w and w + 16, each over all four row
+// groups, so a tile's activation fragment is loaded once per half step and
+// feeds four independent accumulator chains.  Lane (g, t) reads 16-byte chunks
+// 2t, 2t+1 of its rows and of the activation rows, so the MMA k-slots map to
+// columns 16t..16t+15 of the half.  A cluster of C CTAs splits K; each token's base
 // and sign parts meet in shared memory and the cluster's K slices are summed
 // through distributed shared memory, then written to the original token rows.
 #include <cooperative_groups.h>
@@ -157,10 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = lane >> 2, t = lane & 3;
     const int rg = warp & 3, tq = warp >> 2;  // row group, token-tile quarter
     const int r0 = rg * 16 + g;
-    constexpr int NB = (NTB + 3) / 4;       // base tiles tt = 4i + tq
-    constexpr int NS = kMaxS / 4;           // sign tiles q = 4i + tq
+    constexpr int NB = (NTB + 3) / 4;                              // base tiles tt = 4i + tq
+    constexpr int NS = (kMaxS + kConsumerWarps - 1) / kConsumerWarps;  // sign tiles q = 16i + warp
 
-    float accb[NB][4], accs[NS][4];
+    float accb[NB][4], accs[NS][4][4];  // accs[tile][row group][fragment]
 #pragma unroll
     for (int i = 0; i < NB; ++i)
 #pragma unroll
@@ -168,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int i = 0; i < NS; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) accs[i][j] = 0.0f;
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) accs[i][r][j] = 0.0f;
 
     // ---- TMA issue, spread over the warps ----
     // A step's boxes are W(k), W(k+64), x(k), x(k+64) and one bits box per
@@ -208,21 +212,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (; issued < n_steps && issued < R::kStages; ++issued) issue(issued);
     }
     {
-    // Constants of this warp's sign tiles q = 4i + tq (the same in every K step).
+    // Constants of this warp's sign tiles q = 16i + warp (the same in every K step).  A warp
+    // takes a tile over all four row groups, so the tile's activations are read once per
+    // half-step and feed four independent accumulator chains.
     const uint32_t sw0 = static_cast<uint32_t>(((2 * t) ^ g) << 4);      // rows with (row & 7) == g
     const uint32_t sw1 = static_cast<uint32_t>(((2 * t + 1) ^ g) << 4);
-    const int n_mine = n_st > tq ? (n_st - tq + 3) / 4 : 0;
-    const int n_pairs = (n_mine + 1) / 2;
+    const int n_mine = n_st > warp ? (n_st - warp + kConsumerWarps - 1) / kConsumerWarps : 0;
     // A token row past its tile only feeds MMA column g, which the epilogue
     // drops, so it reads some in-box row instead of being zeroed.
     int x_off[NS], b_off[NS];
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
-        const int q = 4 * i + tq;
+        const int q = min(kConsumerWarps * i + warp, kMaxS - 1);  // the table's last entry past its end
         const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1];
         const int xr = min(start + g, MP - 1);
         x_off[i] = xr * 128 + (((2 * t) ^ (xr & 7)) << 4);
-        b_off[i] = v * kBitsBox + r0 * 16 + 2 * t;
+        b_off[i] = v * kBitsBox + g * 16 + 2 * t;  // row group r adds 256 (16 rows of 16 bytes)
     }
 
     bool ok = true;
@@ -240,6 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++issued;
             }
         }
+        // The other lanes wait for lane 0's copies here, not on the full barrier: a lane spinning on
+        // a barrier that only its own warp's lane 0 can complete may hold that lane back for long.
+        __syncwarp();
         const bool got = mbar_wait(&full[s], (i / R::kStages) & 1, a.wait_ns, abort_flag);
         if (!__all_sync(0xFFFFFFFFu, got)) {
             if (lane == 0) {
@@ -275,28 +283,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             }
-            // signs: this warp's tiles in interleaved pairs (a missing second tile is empty)
+            // signs: this warp's tiles, each over the four row groups (rows 16r + g and 16r + g + 8)
 #pragma unroll
-            for (int ip = 0; ip < (NS + 1) / 2; ++ip) {
-                if (ip < n_pairs) {
-                    uint32_t sa[2][8], sb[2][8], xv[2][8];
+            for (int i = 0; i < NS; ++i) {
+                if (i < n_mine) {
+                    const uint4 p0 = lds128(xbox + x_off[i]);
+                    const uint4 p1 = lds128(xbox + (x_off[i] ^ 16));  // chunk 2t+1: flip the chunk's low bit
+                    const uint32_t xv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int i2 = 2 * ip + e < NS ? 2 * ip + e : NS - 1;
-                        signs8(bits + b_off[i2], a.sign_mul, sa[e]);
-                        signs8(bits + b_off[i2] + 128, a.sign_mul, sb[e]);  // row r0 + 8
-                        const uint4 p0 = lds128(xbox + x_off[i2]);
-                        const uint4 p1 = lds128(xbox + (x_off[i2] ^ 16));  // chunk 2t+1: flip the chunk's low bit
-                        xv[e][0] = p0.x, xv[e][1] = p0.y, xv[e][2] = p0.z, xv[e][3] = p0.w;
-                        xv[e][4] = p1.x, xv[e][5] = p1.y, xv[e][6] = p1.z, xv[e][7] = p1.w;
+                    for (int r = 0; r < 4; ++r) {
+                        uint32_t sa[8], sb[8];
+                        signs8(bits + b_off[i] + 256 * r, a.sign_mul, sa);
+                        signs8(bits + b_off[i] + 256 * r + 128, a.sign_mul, sb);  // row + 8
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma_bf16_16816(accs[i][r], sa[2 * j], sb[2 * j], sa[2 * j + 1], sb[2 * j + 1], xv[2 * j],
+                                           xv[2 * j + 1]);
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e)
-                            if (2 * ip + e < NS)
-                                mma_bf16_16816(accs[2 * ip + e], sa[e][2 * j], sb[e][2 * j], sa[e][2 * j + 1],
-                                               sb[e][2 * j + 1], xv[e][2 * j], xv[e][2 * j + 1]);
                 }
             }
         }
@@ -331,19 +334,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < NS; ++i) {  // alpha is constant along k: applied once to the full sign sums
-        const int q = 4 * i + tq;
+        const int q = kConsumerWarps * i + warp;
         if (q < n_st) {
             const int v = tiles_s[3 * q], start = tiles_s[3 * q + 1], cnt = tiles_s[3 * q + 2];
-            const float al0 = alpha_s[v * kRows + r0], al1 = alpha_s[v * kRows + r0 + 8];
-            if (2 * t < cnt) {
-                float *p = red + (start + 2 * t) * kRows + r0;
-                p[0] = (SIGN ? 0.0f : p[0]) + al0 * accs[i][0];
-                p[8] = (SIGN ? 0.0f : p[8]) + al1 * accs[i][2];
-            }
-            if (2 * t + 1 < cnt) {
-                float *p = red + (start + 2 * t + 1) * kRows + r0;
-                p[0] = (SIGN ? 0.0f : p[0]) + al0 * accs[i][1];
-                p[8] = (SIGN ? 0.0f : p[8]) + al1 * accs[i][3];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int row = 16 * r + g;
+                const float al0 = alpha_s[v * kRows + row], al1 = alpha_s[v * kRows + row + 8];
+                if (2 * t < cnt) {
+                    float *p = red + (start + 2 * t) * kRows + row;
+                    p[0] = (SIGN ? 0.0f : p[0]) + al0 * accs[i][r][0];
+                    p[8] = (SIGN ? 0.0f : p[8]) + al1 * accs[i][r][2];
+                }
+                if (2 * t + 1 < cnt) {
+                    float *p = red + (start + 2 * t + 1) * kRows + row;
+                    p[0] = (SIGN ? 0.0f : p[0]) + al0 * accs[i][r][1];
+                    p[8] = (SIGN ? 0.0f : p[8]) + al1 * accs[i][r][3];
+                }
             }
         }
     }

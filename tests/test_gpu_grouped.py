@@ -143,6 +143,23 @@ def test_fourteen_variant_workload_full_size(kind, grouped_path):
     assert_y_close(yh[ts, js], y_ref, mag, f"14-variant {kind}")
 
 
+@pytest.mark.parametrize("m", [1, 8, 16])
+@pytest.mark.parametrize("path", ["2", "4"], ids=["mma_stream", "base_tc_signs_mma"])
+def test_small_batches_on_the_fourteen_variant_shape(m, path, monkeypatch):
+    """Few tokens over the full 8192 x 8192 shape: 64 K steps per CTA with warps that have no
+    sign tile (fewer tiles than warps) running ahead of the others through the ring."""
+    monkeypatch.setenv("BD_GROUPED_PATH", path)
+    c = workloads.GROUPED_14
+    ids = synth.uniform_ids(m, c["n_variants"], c["seed"] + m)
+    case = GroupedCase(c["n_out"], c["n_in"], c["n_variants"], ids, scales=workloads.variant_scales(c),
+                       sigma=c["sigma"], seed=c["seed"])
+    y = case.run()
+    assert bd.bd_get_device_status() == bd.BD_OK
+    ts, js = sample_outputs(case.m, case.n_out, 600, seed=m)
+    y_ref, mag = case.reference_sampled(ts, js)
+    assert_y_close(y_host(y)[ts, js], y_ref, mag, f"14-variant m={m} path={path}")
+
+
 @pytest.fixture(params=["1", "2", "3", "4"], ids=["tcgen05_stream", "mma_stream", "per_variant_tiles",
                                                   "base_tc_signs_mma"])
 def grouped_path(request, monkeypatch):
