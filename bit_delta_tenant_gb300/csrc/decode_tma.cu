@@ -484,19 +484,34 @@ bool decode_tma_multi_supported(const BatchItem *items, int n) {
 // (C = ceil(1.5 * SMs / blocks) while the blocks leave SMs idle; BD_DECODE_CLUSTER overrides).
 struct MultiShape {
     int64_t mmax, blocks, min_steps;
-    int cluster;
+    int cluster, rg;
 };
+// As for one linear, when the 64-row blocks exceed the SMs by less than a factor of two at m <= 8,
+// taller CTAs split in two along K balance the SMs better: R = ceil(groups / SMs) up to 6 (a ring
+// of three stages at two CTAs per SM), C = 2 (3 x 4096^2, m = 1: 18.2 against 19.7 us; at m = 16
+// the shallower ring loses, 26.3 against 23.0, so R stays 4 there).  BD_MULTI_RG overrides R.
 MultiShape multi_shape(const BatchItem *items, int n, const DevCtx &ctx) {
-    MultiShape m{0, 0, -1, 1};
+    MultiShape m{0, 0, -1, 1, 4};
+    int64_t groups = 0, blocks4 = 0;
     for (int i = 0; i < n; ++i) {
         m.mmax = items[i].m > m.mmax ? items[i].m : m.mmax;
-        m.blocks += (items[i].n_out + 63) / 64;
+        groups += (items[i].n_out + 15) / 16;
+        blocks4 += (items[i].n_out + 63) / 64;
         const int64_t st = items[i].n_in / kStepK;
         m.min_steps = m.min_steps < 0 || st < m.min_steps ? st : m.min_steps;
     }
-    int c = m.blocks >= ctx.num_sms
-                ? 1
-                : static_cast<int>((3 * static_cast<int64_t>(ctx.num_sms) / 2 + m.blocks - 1) / m.blocks);
+    int c = 0;
+    const int64_t sms = ctx.num_sms;
+    if (m.mmax <= 8 && blocks4 > sms && blocks4 < 2 * sms) {
+        const int64_t r = (groups + sms - 1) / sms;
+        if (r <= 6) m.rg = static_cast<int>(r), c = 2;
+    }
+    m.rg = env_int("BD_MULTI_RG", m.rg);
+    if (m.rg < 4 || m.rg > 8) m.rg = 4;
+    const int64_t rows = 16 * m.rg;
+    for (int i = 0; i < n; ++i) m.blocks += (items[i].n_out + rows - 1) / rows;
+    if (c == 0 || m.rg == 4)
+        c = m.blocks >= sms ? 1 : static_cast<int>((3 * sms / 2 + m.blocks - 1) / m.blocks);
     c = env_int("BD_DECODE_CLUSTER", c);
     if (c > 8) c = 8;
     if (c > m.min_steps) c = static_cast<int>(m.min_steps);
@@ -507,7 +522,7 @@ MultiShape multi_shape(const BatchItem *items, int n, const DevCtx &ctx) {
 bool decode_tma_multi_one_wave(const BatchItem *items, int n, const DevCtx &ctx) {
     if (!decode_tma_multi_supported(items, n)) return false;
     const MultiShape m = multi_shape(items, n, ctx);
-    return m.blocks * m.cluster <= 2 * static_cast<int64_t>(ctx.num_sms);  // two 64-row CTAs per SM
+    return m.blocks * m.cluster <= 2 * static_cast<int64_t>(ctx.num_sms);  // two CTAs per SM
 }
 
 cudaError_t launch_decode_tma_multi(const BatchItem *items, int n, const DevCtx &ctx, cudaStream_t stream) {
@@ -516,9 +531,11 @@ cudaError_t launch_decode_tma_multi(const BatchItem *items, int n, const DevCtx 
     const int c = ms.cluster;
     TmaPlan p;
     p.nt = ms.mmax <= 8 ? 1 : 2;
-    p.rg = 4;
+    p.rg = plan_instantiated(p.nt, ms.rg) ? ms.rg : 4;
     p.cluster = c;
-    p.stages = p.nt == 1 ? 5 : 4;
+    p.stages = p.rg == 4 ? (p.nt == 1 ? 5 : 4) : stages_within(p.rg, p.nt, kSmemPerSm / 2 - 1024);  // two per SM
+    if (p.stages < 3) return cudaErrorNotSupported;
+    const int64_t rows = 16 * p.rg;
     TmaMaps maps;
     TmaDecodeArgs a{};
     int64_t first = 0;
@@ -527,13 +544,13 @@ cudaError_t launch_decode_tma_multi(const BatchItem *items, int n, const DevCtx 
         const int64_t steps = it.n_in / kStepK;
         const int64_t ks = (steps + c - 1) / c * kStepK;
         if (!fill_linear(maps, a, i, it.x, it.m, it.w_base, it.bits, it.alpha, it.alpha_mode, it.n_out, it.n_in, it.y,
-                         64u, 8 * p.nt, ks, first))
+                         static_cast<uint32_t>(rows), 8 * p.nt, ks, first))
             return cudaErrorInvalidValue;
-        first += (it.n_out + 63) / 64 * c;
+        first += (it.n_out + rows - 1) / rows * c;
     }
     fill_common(a, p, n, ctx);
     if (std::getenv("BD_DECODE_PLAN_VERBOSE"))
-        std::fprintf(stderr, "decode plan, %d linears, m<=%d: R=4 C=%d CTAs=%lld\n", n, 8 * p.nt, c,
+        std::fprintf(stderr, "decode plan, %d linears, m<=%d: R=%d C=%d CTAs=%lld\n", n, 8 * p.nt, p.rg, c,
                      static_cast<long long>(first));
     return launch_any(maps, a, first, p, ctx, stream);
 }

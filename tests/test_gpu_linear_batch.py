@@ -89,6 +89,10 @@ BATCHES = {  # ragged rows (not multiples of 64), several K lengths, both token 
     "ragged": [(200, 384, 3), (65, 1152, 8), (1, 128, 5), (1000, 640, 2)],
     "two_tiles": [(300, 768, 16), (129, 256, 9), (64, 2048, 12)],
     "mixed_tiles": [(96, 1024, 1), (96, 1024, 16), (333, 384, 4), (70, 896, 11)],
+    # m <= 8 with 64-row blocks between one and two per SM: taller CTAs (80 / 96 rows on 152 SMs)
+    # split in two along K, last blocks partial
+    "tall_ctas_r5": [(4000, 512, 2), (4000, 384, 5), (2000, 256, 1)],
+    "tall_ctas_r6": [(4000, 512, 1), (4000, 512, 3), (4000, 640, 8), (200, 256, 6)],
 }
 
 
