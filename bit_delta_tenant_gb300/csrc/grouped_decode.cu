@@ -463,11 +463,12 @@ cudaError_t launch_grouped_decode(const void *x_sorted, int64_t m, const void *w
     // four CTAs only when they fit in one wave (their scheduling costs more).  Fitted to GB300
     // measurements at 64 tokens, 14 variants: 14336 x 4096 164 us with c = 2 against 195 us
     // with c = 1; 4096 x 4096 61 us (c = 2) against 81 us (c = 3); 8192 x 8192 186 us (c = 1)
-    // against 195 / 206 / 255 us (c = 2 / 4 / 8).
+    // against 195 / 206 / 255 us (c = 2 / 4 / 8).  Clusters of 8 (one CTA per SM) cost more than
+    // the model says: 1024 x 4096 takes 39.7 us with c = 8 against 30.2 us with c = 6, so c <= 6.
     const int64_t row_blocks = (n_out + kRows - 1) / kRows;
     const int64_t steps = n_in / kStepK;
     int64_t c = 1, best = -1;
-    for (int64_t cc = 1; cc <= 8 && cc <= steps; ++cc) {
+    for (int64_t cc = 1; cc <= 6 && cc <= steps; ++cc) {
         if (cc > 4 && row_blocks * cc > ctx.num_sms) continue;  // clusters above 4 only in a single wave
         const int64_t cost = (row_blocks * cc + ctx.num_sms - 1) / ctx.num_sms * ((steps + cc - 1) / cc + 3);
         if (best < 0 || cost < best) best = cost, c = cc;
