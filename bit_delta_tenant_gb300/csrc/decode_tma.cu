@@ -479,9 +479,10 @@ bool decode_tma_multi_supported(const BatchItem *items, int n) {
     return true;
 }
 
-// Several linears (m <= 16) in one launch of the cluster-split kernel: 64-row CTAs, two per SM,
-// one K split C for all of them from their blocks together, the same rule as for one linear
-// (C = ceil(1.5 * SMs / blocks) while the blocks leave SMs idle; BD_DECODE_CLUSTER overrides).
+// Several linears (m <= 16) in one launch of the cluster-split kernel: CTAs of R row groups (64
+// rows unless the rule below applies), two per SM, one K split C for all of them from their blocks
+// together, the same rule as for one linear (C = ceil(1.5 * SMs / blocks) while the blocks leave
+// SMs idle; BD_DECODE_CLUSTER overrides).
 struct MultiShape {
     int64_t mmax, blocks, min_steps;
     int cluster, rg;
