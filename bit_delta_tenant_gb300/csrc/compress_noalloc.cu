@@ -28,23 +28,18 @@ static __device__ __align__(256) double g_noalloc_partials[BD_NOALLOC_MAX_PARTIA
 constexpr int kMaxDevices = 128;
 std::mutex g_setup_mu;
 double *g_partials_addr[kMaxDevices] = {nullptr};
-int g_sms[kMaxDevices] = {0};
 
 // Set-up, once per device with that device current: the host-side name of a
 // __device__ array is only a stand-in, so the kernels receive the device
 // address returned by cudaGetSymbolAddress.
-int32_t setup_device(int dev, double **partials, int *num_sms) {
+int32_t setup_device(int dev, double **partials) {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     if (g_partials_addr[dev] == nullptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) return BD_ERR_CUDA;
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return BD_ERR_CUDA;
         g_partials_addr[dev] = static_cast<double *>(p);
-        g_sms[dev] = sms;
     }
     *partials = g_partials_addr[dev];
-    *num_sms = g_sms[dev];
     return BD_OK;
 }
 
@@ -60,21 +55,24 @@ BD_API int32_t bd_compress_noalloc(const void *w_base, const void *w_ft, int64_t
     if (n_in % 8 != 0 || n_out >= BD_MAX_DIM || n_in >= BD_MAX_DIM) return BD_ERR_UNSUPPORTED_SHAPE;
     if (!aligned16(w_base) || !aligned16(w_ft) || !aligned16(bits_out) || !aligned16(alpha_out))
         return BD_ERR_MISALIGNED;
-    // The built-in scratch holds BD_NOALLOC_MAX_PARTIALS partial sums; larger
-    // shapes must use bd_compress with a caller-provided workspace.
+    // The built-in scratch holds BD_NOALLOC_MAX_PARTIALS partial sums; shapes
+    // needing more must use bd_compress with a caller-provided workspace.  A
+    // shape whose rows are one segment each needs none: pass 1 writes alpha.
     const bd::CompressGeom g = bd::compress_geometry(n_out, n_in, alpha_mode);
-    if (g.rows * g.segs > static_cast<int64_t>(BD_NOALLOC_MAX_PARTIALS)) return BD_ERR_WORKSPACE;
+    if (g.segs > 1 && g.rows * g.segs > static_cast<int64_t>(BD_NOALLOC_MAX_PARTIALS)) return BD_ERR_WORKSPACE;
 
     bd::DevCtx ctx;
     int32_t rc = bd::make_dev_ctx(&ctx);  // status word and wait limit, as for bd_compress
     if (rc != BD_OK) return rc;
     if (ctx.device >= kMaxDevices) return BD_ERR_CUDA;
     double *partials = nullptr;
-    int sms = 0;
-    rc = setup_device(ctx.device, &partials, &sms);
+    rc = setup_device(ctx.device, &partials);
     if (rc != BD_OK) return rc;
     // Every partial slot the kernels read is written earlier in the same call
-    // (one slot per block of the first pass), so nothing needs clearing.
+    // (one slot per block of the first pass), so nothing needs clearing.  The
+    // compression kernels are programmatic dependents of the kernel before
+    // them and wait for it before touching the partials, so calls queued on
+    // one stream never overlap on the array.
     const cudaError_t e = bd::launch_compress(w_base, w_ft, n_out, n_in, alpha_mode, bits_out, alpha_out, partials,
                                               ctx, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;

@@ -49,9 +49,11 @@ def _same(got, ref):
 @pytest.mark.parametrize("mode", [0, 1])
 def test_two_calls_in_a_row_match_bd_compress(mode):
     # A large shape first, then a smaller one: the second call must not be
-    # affected by what the first left in the shared scratch.
+    # affected by what the first left in the shared scratch.  Both split their
+    # rows into several segments in either mode (n_in > 8192), so the second
+    # call reads partial-sum slots that the first one wrote.
     a = synth.matrix_pair(4096, 11008, 0.02, 1e-3, seed=101, device="cuda")
-    b = synth.matrix_pair(300, 136, 0.02, "row:5e-4:2e-3", seed=102, device="cuda")
+    b = synth.matrix_pair(300, 8320, 0.02, "row:5e-4:2e-3", seed=102, device="cuda")
     first = _no_alloc(*a, mode)
     second = _no_alloc(*b, mode)
     torch.cuda.synchronize()
@@ -70,8 +72,10 @@ def test_repeated_call_on_same_input_is_identical():
 
 
 def test_shape_beyond_the_built_in_scratch_is_rejected():
-    # per-row alpha with 131073 rows needs 131073 partial sums > BD_NOALLOC_MAX_PARTIALS;
-    # rejected on the host before any launch, so these fake pointers are never touched.
+    # per-row alpha with 65537 rows of 8200 inputs (1025 chunks: two segments per row) needs
+    # 131074 partial sums > BD_NOALLOC_MAX_PARTIALS; rejected on the host before any launch,
+    # so these fake pointers are never touched.
     lib = bd.load_library()
-    rc = lib.bd_compress_noalloc(0x10000, 0x10000, bd.BD_NOALLOC_MAX_PARTIALS + 1, 8, 1, 0x10000, 0x10000, None)
+    rows = bd.BD_NOALLOC_MAX_PARTIALS // 2 + 1
+    rc = lib.bd_compress_noalloc(0x10000, 0x10000, rows, 8200, 1, 0x10000, 0x10000, None)
     assert rc == bd.BD_ERR_WORKSPACE
