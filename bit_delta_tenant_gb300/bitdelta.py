@@ -34,6 +34,12 @@ BD_LINEAR_BATCH_MAX = 256
 BD_COMPRESS_BATCH_MAX = 4096
 BD_COMPRESS_BATCH_PER_LAUNCH = 8
 BD_LINEAR_BATCH_PER_LAUNCH = 8
+BD_OPT_COMPRESS_FORM = 1
+BD_OPT_GROUPED_PATH = 2
+BD_OPT_BATCH_KERNEL = 3
+BD_OPT_BATCH_SINGLE = 4
+BD_OPT_BATCH_GRID = 5
+BD_OPT_TEST_STALL = 6
 
 _lock = threading.Lock()
 _lib = None
@@ -99,6 +105,8 @@ def load_library(path: str | None = None):
         lib.bd_cache_get_stats.restype = I32
         lib.bd_cache_is_resident.argtypes = [V, I32]
         lib.bd_cache_is_resident.restype = I32
+        lib.bd_set_option.argtypes = [I32, I64]
+        lib.bd_set_option.restype = I64
         lib.bd_set_weight_prefetch.argtypes = [I32]
         lib.bd_set_weight_prefetch.restype = I32
         lib.bd_get_device_status.argtypes = [V]
@@ -159,6 +167,27 @@ def bd_set_wait_limit_ns(limit_ns: int) -> int:
 
 def bd_set_linear_path(path: int) -> int:
     return int(load_library().bd_set_linear_path(int(path)))
+
+
+def bd_set_option(option: int, value: int) -> int:
+    """Force one kernel choice (BD_OPT_*); returns the previous value, -1 if rejected."""
+    return int(load_library().bd_set_option(int(option), int(value)))
+
+
+class option:
+    """Context manager: bd_set_option(opt, value) inside, the previous value restored after."""
+
+    def __init__(self, opt: int, value: int):
+        self.opt, self.value = opt, value
+
+    def __enter__(self):
+        self.prev = bd_set_option(self.opt, self.value)
+        if self.prev < 0:
+            raise ValueError(f"bd_set_option({self.opt}, {self.value}) rejected")
+        return self
+
+    def __exit__(self, *exc):
+        bd_set_option(self.opt, self.prev)
 
 
 class CacheStats(ctypes.Structure):

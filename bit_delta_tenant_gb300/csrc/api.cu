@@ -5,7 +5,6 @@
 // (so the library needs no link-time dependency on the driver library).
 #include <algorithm>
 #include <atomic>
-#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -27,21 +26,30 @@ int g_num_sms[kMaxDevices] = {0};
 std::atomic<int64_t> g_wait_ns{-1};
 std::atomic<int32_t> g_linear_path{0};
 std::atomic<int32_t> g_weight_prefetch{0};
+constexpr int kNumOptions = BD_OPT_TEST_STALL + 1;
+std::atomic<int64_t> g_options[kNumOptions] = {};
 
 int64_t wait_limit_ns() {
     int64_t v = g_wait_ns.load();
     if (v < 0) {
-        int64_t init = 2000000000LL;
-        if (const char *e = std::getenv("BD_WAIT_LIMIT_NS")) {
-            char *end = nullptr;
-            long long p = std::strtoll(e, &end, 10);
-            if (end != e && p >= 0) init = p;
-        }
         int64_t expected = -1;
-        g_wait_ns.compare_exchange_strong(expected, init);
+        g_wait_ns.compare_exchange_strong(expected, 2000000000LL);  // 2 s
         v = g_wait_ns.load();
     }
     return v;
+}
+
+// Largest value each bd_set_option knob accepts (index = BD_OPT_*).
+int64_t option_max(int32_t option) {
+    switch (option) {
+        case BD_OPT_COMPRESS_FORM: return 1;
+        case BD_OPT_GROUPED_PATH: return 4;
+        case BD_OPT_BATCH_KERNEL: return 2;
+        case BD_OPT_BATCH_SINGLE: return 1;
+        case BD_OPT_BATCH_GRID: return 0x7FFFFFFFLL;
+        case BD_OPT_TEST_STALL: return 1;
+        default: return -1;
+    }
 }
 
 int32_t make_ctx(bd::DevCtx *ctx) {
@@ -63,6 +71,7 @@ int32_t make_ctx(bd::DevCtx *ctx) {
     ctx->device = dev;
     ctx->weight_prefetch = g_weight_prefetch.load() != 0;
     ctx->wait_ns = static_cast<uint64_t>(wait_limit_ns());
+    ctx->test_stall = g_options[BD_OPT_TEST_STALL].load() != 0;
     return BD_OK;
 }
 
@@ -85,6 +94,10 @@ int32_t check_matrix_shape(int64_t n_out, int64_t n_in) {
 namespace bd {
 
 int32_t make_dev_ctx(DevCtx *ctx) { return make_ctx(ctx); }
+
+int64_t option_value(int32_t option) {
+    return option > 0 && option < kNumOptions ? g_options[option].load() : 0;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -146,6 +159,12 @@ BD_API int32_t bd_set_linear_path(int32_t path) {
     const int32_t prev = g_linear_path.load();
     if (path >= 0 && path <= 3) g_linear_path.store(path);
     return prev;
+}
+
+BD_API int64_t bd_set_option(int32_t option, int64_t value) {
+    const int64_t mx = option_max(option);
+    if (mx < 0 || value < 0 || value > mx) return -1;
+    return g_options[option].exchange(value);
 }
 
 BD_API int32_t bd_set_weight_prefetch(int32_t enable) {
@@ -315,9 +334,8 @@ int32_t schedule_batch(const bd_linear_desc *d, int32_t n, BatchSchedule &out) {
     }
     const int32_t path = g_linear_path.load();
     // A launch of one linear gains nothing from the shared split: it runs as bd_linear
-    // (the cluster-split kernel) unless BD_BATCH_SINGLE=1 keeps it (measurements).
-    const char *single_env = std::getenv("BD_BATCH_SINGLE");
-    const size_t min_size = single_env != nullptr && single_env[0] == '1' ? 1 : 2;
+    // (the cluster-split kernel) unless the BD_OPT_BATCH_SINGLE option keeps it (tests).
+    const size_t min_size = bd::option_value(BD_OPT_BATCH_SINGLE) == 1 ? 1 : 2;
     std::vector<int32_t> group[2];  // problems of the batched kernel, by token tiles
     for (int32_t i = 0; i < n; ++i) {
         const bd_linear_desc &q = d[i];
@@ -393,12 +411,12 @@ BD_API int32_t bd_linear_batch(const bd_linear_desc *descs, int32_t n, void *wor
     // Launches share the workspace: each one's accesses follow the previous one's completion on the stream.
     // Kernel per launch: the cluster-split kernel when its CTAs fit in one wave (measured faster
     // there, e.g. 3 x 4096^2 at m = 1: 19.7 against 22.8 us), else the evenly split one (2 x
-    // 11008x4096: 33.8 against 41.4 us); BD_BATCH_KERNEL=cluster|streamk forces one (measurements).
-    const char *kern = std::getenv("BD_BATCH_KERNEL");
+    // 11008x4096: 33.8 against 41.4 us); the BD_OPT_BATCH_KERNEL option forces one (tests).
+    const int64_t kern = bd::option_value(BD_OPT_BATCH_KERNEL);
     for (size_t i = 0; i < sch.launches.size(); ++i) {
         const bd::BatchItem *items = sch.launches[i].data();
         const int cnt = static_cast<int>(sch.launches[i].size());
-        const bool cluster = kern != nullptr ? kern[0] == 'c' : bd::decode_tma_multi_one_wave(items, cnt, ctx);
+        const bool cluster = kern != 0 ? kern == 1 : bd::decode_tma_multi_one_wave(items, cnt, ctx);
         const int32_t r = cluster && bd::decode_tma_multi_supported(items, cnt)
                               ? cuda_status(bd::launch_decode_tma_multi(items, cnt, ctx, s))
                               : cuda_status(bd::launch_decode_batch(items, cnt, plans[i], workspace, ctx, s));

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "bitdelta.h"
+
 namespace bd {
 
 // Bits of the sticky device status word (set with atomicOr by kernels, read
@@ -22,7 +24,11 @@ struct DevCtx {
     int num_sms;          // SM count of the current device
     int device;           // current device ordinal
     bool weight_prefetch; // weights may be read before the preceding kernel on the stream completes
+    bool test_stall;      // BD_OPT_TEST_STALL: a first pipeline wait on a barrier nothing completes
 };
+
+// Current value of a bd_set_option knob (BD_OPT_*; 0 = automatic).
+int64_t option_value(int32_t option);
 
 // Device context of the current device (status word address, SM count, the
 // process-wide wait limit); returns a bd_status code.

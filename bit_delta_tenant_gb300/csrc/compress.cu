@@ -43,6 +43,7 @@ struct CompressArgs {
     double count;      // elements per row: alpha = sum / count
     int64_t row_chunks;
     int64_t segs;
+    int32_t test_stall;  // ring form: the first consumer wait is on a barrier nothing completes (tests)
 };
 
 // Signs and |Delta| of one chunk: returns the packed byte and the pairwise
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
     uint64_t *empty = full + kRingStages;
     double *warp_sum = reinterpret_cast<double *>(empty + kRingStages);  // [2][8]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(warp_sum + 16);
+    uint64_t *never = reinterpret_cast<uint64_t *>(warp_sum + 17);  // completed by no one
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCompressThreads / 32);
         }
+        mbar_init(never, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -170,7 +173,8 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
         for (int u = 0; u < kCompressChunksPerThread; ++u) cs[u] = 0.0f;
         for (int h = 0; h * kHalfChunks < n; ++h, ++j) {
             const int st = j % kRingStages;
-            const bool got = mbar_wait(&full[st], (j / kRingStages) & 1, wait_ns, abort_flag);
+            const bool got = mbar_wait(a.test_stall && j == 0 ? never : &full[st], (j / kRingStages) & 1, wait_ns,
+                                       abort_flag);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 if (lane == 0) {
                     *abort_flag = 1;
@@ -414,6 +418,7 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
     a.count = static_cast<double>(g.row_chunks) * 8.0;
     a.row_chunks = g.row_chunks;
     a.segs = g.segs;
+    a.test_stall = ctx.test_stall ? 1 : 0;
     const int64_t n_segs = g.rows * g.segs;
     static bool attr_set[128] = {false};
     if (ctx.device >= 0 && ctx.device < 128 && !attr_set[ctx.device]) {
@@ -422,13 +427,12 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
-    // The direct form (one block per segment) unless BD_COMPRESS_RING=1 selects
-    // the persistent ring form.  Measured on GB300 (graph-replayed): the direct
+    // The direct form (one block per segment) unless the BD_OPT_COMPRESS_FORM
+    // option selects the persistent ring form.  Measured on GB300 (graph-replayed): the direct
     // form is 4% faster on the Llama-7B layer step and up to 15% on per-row
     // compressions, the ring form 2-3% faster on scalar compressions of
     // 8192 x 8192 and 11008 x 4096; both give the same bits and alpha.
-    const char *ring_env = std::getenv("BD_COMPRESS_RING");
-    const bool ring = ring_env != nullptr && ring_env[0] == '1';
+    const bool ring = option_value(BD_OPT_COMPRESS_FORM) == 1;
     const int64_t grid = ring ? (n_segs < 2 * ctx.num_sms ? n_segs : 2 * ctx.num_sms) : n_segs;
     if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
@@ -482,6 +486,7 @@ cudaError_t launch_compress_batch(const CompressItem *items, int n, const DevCtx
         a.count = static_cast<double>(g.row_chunks) * 8.0;
         a.row_chunks = g.row_chunks;
         a.segs = g.segs;
+        a.test_stall = 0;  // the direct form has no pipeline waits
         a1.first_block[i] = blocks1;
         blocks1 += g.rows * g.segs;
         if (g.segs > 1) {  // pass 2 only for rows split into several segments

@@ -395,15 +395,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// Ring depth: the deepest that keeps two CTAs per SM (BD_BATCH_STAGES overrides, for sweeps).
-int stages_for(int nt) {
-    static const int forced = [] {
-        const char *e = std::getenv("BD_BATCH_STAGES");
-        return e != nullptr ? std::atoi(e) : 0;
-    }();
-    if (forced >= 2 && forced <= 12) return forced;
-    return nt == 1 ? 5 : 4;
-}
+// Ring depth: the deepest that keeps two CTAs per SM.
+int stages_for(int nt) { return nt == 1 ? 5 : 4; }
 
 size_t smem_for(int nt) {
     const StageLayout L = stage_layout(kRG, nt);
@@ -452,10 +445,8 @@ BatchPlan plan_decode_batch(const BatchItem *items, int n, const DevCtx &ctx) {
     const int per_sm = pl.nt == 1 ? resident_per_sm<1>() : resident_per_sm<2>();
     if (per_sm < 1 || total < 1) return pl;
     int64_t grid = static_cast<int64_t>(per_sm) * ctx.num_sms;
-    if (const char *e = std::getenv("BD_BATCH_GRID")) {  // sweeps: CTAs per launch
-        const int64_t v = std::atoll(e);
-        if (v > 0) grid = v;
-    }
+    const int64_t forced = option_value(BD_OPT_BATCH_GRID);  // tests: CTAs per launch
+    if (forced > 0) grid = forced;
     // every CTA resident at once: an owner may wait for the CTAs after it
     const int64_t resident = static_cast<int64_t>(per_sm) * ctx.num_sms;
     if (grid > resident) grid = resident;

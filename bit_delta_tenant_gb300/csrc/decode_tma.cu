@@ -258,7 +258,13 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
     // ---- add this rank's rows over the cluster in rank order and write y ----
     const int mine = owned(rank);
     if (mine == 0) return;
-    if (!mbar_wait(inbox_bar, 0, a.wait_ns + kDrainLimitNs, nullptr)) {  // peers always push: bounded drain
+    // Peers push unconditionally (also after a timeout of their own), so this wait runs out only
+    // if a peer has stalled for the wait limit plus a further second.  The kernel then flags a
+    // timeout and this CTA exits without the closing cluster barrier that would otherwise order
+    // late pushes before its exit: a push still in flight may then land in the shared memory the
+    // SM hands to a later CTA.  The status word reports the launch as failed in that case, and
+    // no closing barrier is paid in the normal case (measured: it costs every launch its tail).
+    if (!mbar_wait(inbox_bar, 0, a.wait_ns + kDrainLimitNs, nullptr)) {
         if (ctid == 0) flag_status(a.status, kDevTimeout);
         return;
     }
@@ -280,13 +286,6 @@ struct TmaPlan {
     int nt, cluster, rg, stages;
     int64_t ks, row_blocks;
 };
-
-int env_int(const char *name, int dflt) {
-    const char *e = std::getenv(name);
-    if (!e) return dflt;
-    const int v = std::atoi(e);
-    return v > 0 ? v : dflt;
-}
 
 template <int NT, int RG>
 cudaError_t ensure_smem_attr(int device) {
@@ -327,8 +326,6 @@ int stages_within(int rg, int nt, size_t budget) {
 //    the SMs in one wave -- the MMA work per byte has grown (8192 x 8192:
 //    35.6 us against 44.5 us with R = 4); otherwise as below.
 //  * 32 < m <= 64: R = 4, one CTA per SM.
-// BD_DECODE_ROW_GROUPS / BD_DECODE_CLUSTER / BD_DECODE_STAGES override the
-// three choices (sweeps).
 bool make_tma_plan(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx, TmaPlan &p) {
     const int num_sms = ctx.num_sms;
     if (m < 1 || m > kDecodeMaxM || n_out < 1 || n_in < 1 || num_sms < 1) return false;
@@ -352,14 +349,11 @@ bool make_tma_plan(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx, Tm
             stages = stages_within(rg, p.nt, kSmemPerSm / 2 - 1024);
         }
     }
-    rg = env_int("BD_DECODE_ROW_GROUPS", rg);
     if (!plan_instantiated(p.nt, rg)) rg = 4;
     const int64_t blocks = (groups + rg - 1) / rg;
     if (c == 0) c = blocks >= num_sms ? 1 : static_cast<int>((3 * static_cast<int64_t>(num_sms) / 2 + blocks - 1) / blocks);
-    c = env_int("BD_DECODE_CLUSTER", c);
     if (c > 8) c = 8;
     if (c > steps) c = static_cast<int>(steps);
-    stages = env_int("BD_DECODE_STAGES", stages);
     const int deepest = stages_within(rg, p.nt, kMaxSmem);
     if (stages > deepest) stages = deepest;
     if (stages < 3) return false;
@@ -370,10 +364,6 @@ bool make_tma_plan(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx, Tm
     p.cluster = static_cast<int>((steps + per - 1) / per);  // no empty ranks
     p.row_blocks = blocks;
     if (p.row_blocks * p.cluster > 0x7FFFFFFFLL) return false;
-    if (std::getenv("BD_DECODE_PLAN_VERBOSE"))  // debug: the plan of every launch
-        std::fprintf(stderr, "decode plan m<=%d %lldx%lld: R=%d C=%d stages=%d CTAs=%lld\n", 8 * p.nt,
-                     static_cast<long long>(n_out), static_cast<long long>(n_in), p.rg, p.cluster, p.stages,
-                     static_cast<long long>(p.row_blocks * p.cluster));
     return true;
 }
 
@@ -507,13 +497,11 @@ MultiShape multi_shape(const BatchItem *items, int n, const DevCtx &ctx) {
         const int64_t r = (groups + sms - 1) / sms;
         if (r <= 6) m.rg = static_cast<int>(r), c = 2;
     }
-    m.rg = env_int("BD_MULTI_RG", m.rg);
     if (m.rg < 4 || m.rg > 8) m.rg = 4;
     const int64_t rows = 16 * m.rg;
     for (int i = 0; i < n; ++i) m.blocks += (items[i].n_out + rows - 1) / rows;
     if (c == 0 || m.rg == 4)
         c = m.blocks >= sms ? 1 : static_cast<int>((3 * sms / 2 + m.blocks - 1) / m.blocks);
-    c = env_int("BD_DECODE_CLUSTER", c);
     if (c > 8) c = 8;
     if (c > m.min_steps) c = static_cast<int>(m.min_steps);
     m.cluster = c < 1 ? 1 : c;
@@ -550,9 +538,6 @@ cudaError_t launch_decode_tma_multi(const BatchItem *items, int n, const DevCtx 
         first += (it.n_out + rows - 1) / rows * c;
     }
     fill_common(a, p, n, ctx);
-    if (std::getenv("BD_DECODE_PLAN_VERBOSE"))
-        std::fprintf(stderr, "decode plan, %d linears, m<=%d: R=%d C=%d CTAs=%lld\n", n, 8 * p.nt, p.rg, c,
-                     static_cast<long long>(first));
     return launch_any(maps, a, first, p, ctx, stream);
 }
 

@@ -225,8 +225,8 @@ cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const v
     if (e != cudaSuccess) return e;
 
     // Small batches (default): the mma.sync streaming kernel computing the base
-    // and every variant's sign products in one pass.  BD_GROUPED_PATH=1/2/3/4
-    // forces the tcgen05 streaming kernel / that default / per-variant
+    // and every variant's sign products in one pass.  The BD_OPT_GROUPED_PATH
+    // option 1/2/3/4 forces the tcgen05 streaming kernel / that default / per-variant
     // tensor-core tiles / a split in which the tensor-core kernel computes the
     // base product (fp32, W_base as stored) and the streaming kernel only the
     // sign products (tests and comparisons; unsupported shapes fall through).
@@ -234,8 +234,7 @@ cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const v
     // kernel (195 us for 8192 x 8192), the sign products dominate; the tcgen05
     // streaming kernel issues ~4 N=16 MMAs per variant and K block, each
     // behind an mbarrier round trip, and ends up latency-bound.
-    const char *force = std::getenv("BD_GROUPED_PATH");
-    const int path = force ? std::atoi(force) : 0;
+    const int path = static_cast<int>(option_value(BD_OPT_GROUPED_PATH));
     if (path == 1 && grouped_decode_tc_supported(m, vars.count, n_in, xs, w_base, vars))
         return launch_grouped_decode_tc(xs, m, w_base, vars, n_out, n_in, y, s.seg, s.perm, ctx, stream);
     if (path == 4 && m <= 64 && grouped_decode_supported(m, vars.count, n_in, w_base, vars)) {

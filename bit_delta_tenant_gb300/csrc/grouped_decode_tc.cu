@@ -65,6 +65,7 @@ struct GtcArgs {
     int32_t cluster;
     unsigned *status;
     uint64_t wait_ns;
+    int32_t test_stall;      // the MMA issuer's first wait is on a barrier nothing completes (tests)
 };
 
 struct VarTab {              // active variants in order
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdec_tc_kernel(const __grid_const
     uint64_t *acc_full = a_empty + kMaxABuf;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint64_t *never = reinterpret_cast<uint64_t *>(tmem_slot + 2);  // completed by no one
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdec_tc_kernel(const __grid_const
             mbar_init(&a_empty[b], 1);
         }
         mbar_init(acc_full, 1);
+        mbar_init(never, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -203,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdec_tc_kernel(const __grid_const
             int j = 0;  // running sign-tile counter (A buffer j % nbuf)
             for (int kb = 0; kb < nkb && ok; ++kb) {
                 const int s = kb % kStages;
-                if (!mbar_wait(&full[s], (kb / kStages) & 1, a.wait_ns, abort_flag)) {
+                if (!mbar_wait(a.test_stall && kb == 0 ? never : &full[s], (kb / kStages) & 1, a.wait_ns,
+                               abort_flag)) {
                     give_up(abort_flag, a.status);
                     break;
                 }
@@ -387,6 +391,7 @@ cudaError_t launch_grouped_decode_tc(const void *x_sorted, int64_t m, const void
     a.n_in = n_in;
     a.status = ctx.status;
     a.wait_ns = ctx.wait_ns;
+    a.test_stall = ctx.test_stall ? 1 : 0;
     const int64_t row_tiles = (n_out + kBM - 1) / kBM;
     const int64_t kblocks = n_in / kBK;
     int64_t c = row_tiles >= ctx.num_sms ? 1 : ctx.num_sms / row_tiles;  // fill the SMs without a second wave

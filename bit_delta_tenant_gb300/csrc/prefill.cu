@@ -446,17 +446,11 @@ cudaError_t set_smem_attr(const DevCtx &ctx) {
     return cudaSuccess;
 }
 
-// The rebuilt W tile feeds the MMA from tensor memory by default (measured
-// ~19% faster on GB300 than writing it back to shared memory, which then
-// carries only the TMA fills, the rebuild reads and the activation operand);
-// BD_PREFILL_TMEM_A=0 selects the shared-memory form.
-bool use_tmem_a() {
-    static const bool v = [] {
-        const char *e = std::getenv("BD_PREFILL_TMEM_A");
-        return !(e != nullptr && e[0] == '0');
-    }();
-    return v;
-}
+// The rebuilt W tile feeds the MMA from tensor memory (measured ~19% faster
+// on GB300 than writing it back to shared memory, which then carries only the
+// TMA fills, the rebuild reads and the activation operand); the shared-memory
+// form serves the base-only product, whose A tile is used as loaded.
+constexpr bool use_tmem_a() { return true; }
 
 void fill_common(PrefillArgs &a, int64_t m, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx) {
     a.y = static_cast<uint16_t *>(y);
@@ -505,10 +499,6 @@ cudaError_t launch_prefill_bn(const void *x, int64_t m, const void *w_base, cons
     // ~90% of the SMs are counted on), each rank keeping at least 8 K blocks.
     int c = 1;
     while (c < 8 && tiles * (2 * c) * 10 <= 9 * static_cast<int64_t>(ctx.num_sms) && a.num_kb / (2 * c) >= 8) c *= 2;
-    if (const char *ev = std::getenv("BD_PREFILL_KSPLIT")) {
-        const int f = std::atoi(ev);
-        if (f == 1 || f == 2 || f == 4 || f == 8) c = f;
-    }
     a.kb_per = (a.num_kb + c - 1) / c;
     a.ksplit = (a.num_kb + a.kb_per - 1) / a.kb_per;  // no empty ranks
     const int64_t grid = tiles * a.ksplit;

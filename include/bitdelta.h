@@ -150,11 +150,13 @@ int32_t bd_compress_batch(const bd_compress_desc *descs, int32_t n, void *worksp
  * Same arguments, results and errors as bd_compress, minus the workspace:
  * the partial sums live in a fixed scratch array built into the library,
  * BD_NOALLOC_MAX_PARTIALS doubles (1 MiB) per GPU that loads the library,
- * held until the process exits.  A shape fits when
- *   rows * ceil(chunks / 1024) <= BD_NOALLOC_MAX_PARTIALS,
- * with rows = 1 and chunks = n_out*n_in/8 for a scalar alpha (up to 2^30
- * elements), or rows = n_out and chunks = n_in/8 per row; larger shapes
- * return BD_ERR_WORKSPACE before launching anything (use bd_compress).
+ * held until the process exits.  With rows = 1 and chunks = n_out*n_in/8
+ * for a scalar alpha, or rows = n_out and chunks = n_in/8 per row, and
+ * segs = ceil(chunks / 1024), a shape fits when segs == 1 (each row is one
+ * segment and needs no partial sums) or
+ *   rows * segs <= BD_NOALLOC_MAX_PARTIALS
+ * (a scalar alpha over up to 2^30 elements); larger shapes return
+ * BD_ERR_WORKSPACE before launching anything (use bd_compress).
  * The call allocates and frees nothing.  Its first call on a device looks
  * up the scratch array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  All
@@ -415,6 +417,46 @@ int32_t bd_set_linear_path(int32_t path);
  * bits (for instance, not right after the bd_compress that produces the
  * bits).  Default 0.  Returns the previous setting. */
 int32_t bd_set_weight_prefetch(int32_t enable);
+
+/* Test knob: forces one of the library's kernel choices for calls made
+ * afterwards by this process (every choice computes the same result within
+ * the documented tolerance, and the compression forms the same bits and
+ * alpha bit for bit).  `option` is one of the BD_OPT_* values below, `value`
+ * one of the values listed beside it; 0 always restores the automatic
+ * choice.  Returns the previous value, or -1 (nothing changed) for an
+ * unknown option or a value out of range.  Not synchronised with calls in
+ * flight on other host threads.
+ *   BD_OPT_COMPRESS_FORM  0 one block per segment; 1 the persistent form
+ *                         with a shared-memory copy ring
+ *   BD_OPT_GROUPED_PATH   0 automatic; 1 the tcgen05 streaming kernel;
+ *                         2 the mma.sync streaming kernel; 3 per-variant
+ *                         tensor-core tiles; 4 base product on the tensor
+ *                         cores, sign products on the streaming kernel
+ *                         (paths that cannot run a shape fall through to
+ *                         the automatic choice)
+ *   BD_OPT_BATCH_KERNEL   bd_linear_batch launches: 0 automatic; 1 the
+ *                         cluster-split kernel; 2 the evenly split kernel
+ *   BD_OPT_BATCH_SINGLE   1 keeps a bd_linear_batch group of one problem on
+ *                         the batched kernel instead of running it as
+ *                         bd_linear
+ *   BD_OPT_BATCH_GRID     CTAs of an evenly split batched launch (1 ..
+ *                         2^31-1, capped at the CTAs that fit at once)
+ *   BD_OPT_TEST_STALL     1 makes the first pipeline wait of the kernels
+ *                         that support it -- the persistent compression
+ *                         form and the multi-tenant streaming kernels --
+ *                         wait on a barrier that nothing completes, so that
+ *                         the wait runs out after the wait limit and the
+ *                         kernel takes its give-up path (tests of failure
+ *                         detection; results are then undefined and
+ *                         bd_get_device_status reports
+ *                         BD_ERR_DEVICE_TIMEOUT) */
+#define BD_OPT_COMPRESS_FORM 1
+#define BD_OPT_GROUPED_PATH 2
+#define BD_OPT_BATCH_KERNEL 3
+#define BD_OPT_BATCH_SINGLE 4
+#define BD_OPT_BATCH_GRID 5
+#define BD_OPT_TEST_STALL 6
+int64_t bd_set_option(int32_t option, int64_t value);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t bd_version(void);

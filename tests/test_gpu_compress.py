@@ -63,13 +63,10 @@ def test_hand_worked_bytes_on_gpu(case):
 
 
 @pytest.fixture(params=["direct", "ring"])
-def compress_form(request, monkeypatch):
+def compress_form(request):
     """Both forms of pass 1 (the default direct one, and the persistent ring one)."""
-    if request.param == "ring":
-        monkeypatch.setenv("BD_COMPRESS_RING", "1")
-    else:
-        monkeypatch.delenv("BD_COMPRESS_RING", raising=False)
-    return request.param
+    with bd.option(bd.BD_OPT_COMPRESS_FORM, 1 if request.param == "ring" else 0):
+        yield request.param
 
 
 @pytest.mark.parametrize("n_out,n_in", [(1, 8), (7, 24), (33, 120), (129, 136), (128, 4096), (3, 16392)])
@@ -113,13 +110,13 @@ def test_alpha_is_bitwise_reproducible(mode):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-def test_direct_and_ring_forms_agree_bitwise(mode, monkeypatch):
+def test_direct_and_ring_forms_agree_bitwise(mode):
     """The two forms of pass 1 take the same summation tree, so their alpha agree to the bit."""
     w_base, w_ft = synth.matrix_pair(2048, 11008, 0.02, 1e-3, seed=8, device="cuda")
-    monkeypatch.delenv("BD_COMPRESS_RING", raising=False)
-    b1, a1 = gpu_compress(w_base, w_ft, mode)
-    monkeypatch.setenv("BD_COMPRESS_RING", "1")
-    b2, a2 = gpu_compress(w_base, w_ft, mode)
+    with bd.option(bd.BD_OPT_COMPRESS_FORM, 0):
+        b1, a1 = gpu_compress(w_base, w_ft, mode)
+    with bd.option(bd.BD_OPT_COMPRESS_FORM, 1):
+        b2, a2 = gpu_compress(w_base, w_ft, mode)
     assert torch.equal(b1, b2)
     assert torch.equal(a1.view(torch.int32), a2.view(torch.int32))
 
@@ -210,3 +207,24 @@ def test_batched_compression_of_the_llama3_8b_stack_shapes():
         assert np.array_equal(bits.cpu().numpy(), oracle.sign_bits(wb, wf))
         a64 = oracle.alpha(wb, wf, mode)
         assert abs(float(alpha[0]) - a64[0]) / abs(a64[0]) <= ALPHA_REL
+
+
+def test_stalled_wait_ring_form_reports_timeout_and_context_survives():
+    """The persistent ring form of pass 1, its consumers made to wait first on a barrier that
+    nothing completes (BD_OPT_TEST_STALL) under a 1 ms wait limit, gives up: it records a
+    timeout, its producer drains the copies it issued, and the next call is correct.  (A zero
+    wait limit alone does not force this: the hardware's suspended try-wait outlasts the
+    copy of one ring slot.)"""
+    w_base, w_ft = synth.matrix_pair(2048, 8192, 0.02, 1e-3, seed=61, device="cuda")
+    assert bd.bd_get_device_status() == bd.BD_OK
+    with bd.option(bd.BD_OPT_COMPRESS_FORM, 1):
+        prev = bd.bd_set_wait_limit_ns(1_000_000)
+        try:
+            with bd.option(bd.BD_OPT_TEST_STALL, 1):
+                gpu_compress(w_base, w_ft, 0)
+            status = bd.bd_get_device_status()
+        finally:
+            bd.bd_set_wait_limit_ns(prev)
+        assert status == bd.BD_ERR_DEVICE_TIMEOUT
+        assert bd.bd_get_device_status() == bd.BD_OK
+        check_against_oracle(w_base, w_ft, 0)

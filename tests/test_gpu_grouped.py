@@ -145,15 +145,15 @@ def test_fourteen_variant_workload_full_size(kind, grouped_path):
 
 @pytest.mark.parametrize("m", [1, 8, 16])
 @pytest.mark.parametrize("path", ["2", "4"], ids=["mma_stream", "base_tc_signs_mma"])
-def test_small_batches_on_the_fourteen_variant_shape(m, path, monkeypatch):
+def test_small_batches_on_the_fourteen_variant_shape(m, path):
     """Few tokens over the full 8192 x 8192 shape: 64 K steps per CTA with warps that have no
     sign tile (fewer tiles than warps) running ahead of the others through the ring."""
-    monkeypatch.setenv("BD_GROUPED_PATH", path)
     c = workloads.GROUPED_14
     ids = synth.uniform_ids(m, c["n_variants"], c["seed"] + m)
     case = GroupedCase(c["n_out"], c["n_in"], c["n_variants"], ids, scales=workloads.variant_scales(c),
                        sigma=c["sigma"], seed=c["seed"])
-    y = case.run()
+    with bd.option(bd.BD_OPT_GROUPED_PATH, int(path)):
+        y = case.run()
     assert bd.bd_get_device_status() == bd.BD_OK
     ts, js = sample_outputs(case.m, case.n_out, 600, seed=m)
     y_ref, mag = case.reference_sampled(ts, js)
@@ -162,10 +162,10 @@ def test_small_batches_on_the_fourteen_variant_shape(m, path, monkeypatch):
 
 @pytest.fixture(params=["1", "2", "3", "4"], ids=["tcgen05_stream", "mma_stream", "per_variant_tiles",
                                                   "base_tc_signs_mma"])
-def grouped_path(request, monkeypatch):
+def grouped_path(request):
     """Force one multi-tenant kernel (shapes a kernel cannot take fall through to the next)."""
-    monkeypatch.setenv("BD_GROUPED_PATH", request.param)
-    return request.param
+    with bd.option(bd.BD_OPT_GROUPED_PATH, int(request.param)):
+        yield request.param
 
 
 @pytest.mark.parametrize("n_out,n_in,m,n_var", [(129, 256, 64, 14), (64, 1152, 1, 3), (300, 128, 33, 16),
@@ -188,3 +188,28 @@ def test_streaming_kernel_bad_id_and_empty_variants(grouped_path):
     y_ref, mag = oracle.linear_grouped(case.x_h[good], ids[good], case.wb_h, case.bits_h, case.alpha_h,
                                        np.array(case.modes, np.int32))
     assert_y_close(y_host(y)[good], y_ref, mag, "good tokens (streaming)")
+
+
+@pytest.mark.parametrize("path", ["1", "2", "4"], ids=["tcgen05_stream", "mma_stream", "base_tc_signs_mma"])
+def test_stalled_wait_reports_timeout_and_context_survives(path):
+    """Each multi-tenant streaming kernel, made to wait first on a barrier that nothing
+    completes (BD_OPT_TEST_STALL) under a 1 ms wait limit, gives up: it records a timeout,
+    drains its own copies (and MMAs) and returns.  The status is read and cleared once, the
+    context stays usable, and the same call afterwards is correct against the oracle."""
+    ids = synth.uniform_ids(16, 5, seed=77)
+    case = GroupedCase(1024, 4096, 5, ids, seed=78)
+    assert bd.bd_get_device_status() == bd.BD_OK
+    with bd.option(bd.BD_OPT_GROUPED_PATH, int(path)):
+        prev = bd.bd_set_wait_limit_ns(1_000_000)
+        try:
+            with bd.option(bd.BD_OPT_TEST_STALL, 1):
+                case.run()
+            status = bd.bd_get_device_status()
+        finally:
+            bd.bd_set_wait_limit_ns(prev)
+        assert status == bd.BD_ERR_DEVICE_TIMEOUT
+        assert bd.bd_get_device_status() == bd.BD_OK  # read-and-clear
+        y = case.run()
+    assert bd.bd_get_device_status() == bd.BD_OK
+    y_ref, mag = case.reference()
+    assert_y_close(y_host(y), y_ref, mag, f"after timeout, path {path}")

@@ -56,32 +56,20 @@ def check_all(cases, ys, what):
 KERNELS = ["auto", "cluster", "streamk"]
 
 
+BATCH_KERNEL_VALUE = {"auto": 0, "cluster": 1, "streamk": 2}
+
+
 @pytest.fixture(params=KERNELS)
-def batch_kernel(request, monkeypatch):
+def batch_kernel(request):
     """The kernel a launch of the batch runs: the library's choice (the cluster-split kernel when
-    its CTAs fit in one wave, else the evenly split one) or either one forced (BD_BATCH_KERNEL)."""
-    if request.param == "auto":
-        monkeypatch.delenv("BD_BATCH_KERNEL", raising=False)
-    else:
-        monkeypatch.setenv("BD_BATCH_KERNEL", request.param)
-    return request.param
+    its CTAs fit in one wave, else the evenly split one) or either one forced (BD_OPT_BATCH_KERNEL)."""
+    with bd.option(bd.BD_OPT_BATCH_KERNEL, BATCH_KERNEL_VALUE[request.param]):
+        yield request.param
 
 
-class grid_override:
-    """Forces the number of CTAs of the batched kernel (BD_BATCH_GRID)."""
-
-    def __init__(self, grid):
-        self.grid = grid
-
-    def __enter__(self):
-        self.prev = os.environ.get("BD_BATCH_GRID")
-        os.environ["BD_BATCH_GRID"] = str(self.grid)
-
-    def __exit__(self, *exc):
-        if self.prev is None:
-            os.environ.pop("BD_BATCH_GRID", None)
-        else:
-            os.environ["BD_BATCH_GRID"] = self.prev
+def grid_override(grid):
+    """Forces the number of CTAs of the batched kernel (BD_OPT_BATCH_GRID)."""
+    return bd.option(bd.BD_OPT_BATCH_GRID, grid)
 
 
 BATCHES = {  # ragged rows (not multiples of 64), several K lengths, both token tiles
@@ -106,26 +94,26 @@ def test_batches_match_oracle(name, mode, batch_kernel):
 
 
 @pytest.mark.parametrize("grid", [1, 2, 3, 7, 50, 1000, 100000])
-def test_forced_grids(grid, monkeypatch):
+def test_forced_grids(grid):
     """Few CTAs (every block in one CTA's range, several linears per CTA) to far
     more CTAs than items (capped at one item per CTA: every block split K-step by K-step)."""
-    monkeypatch.setenv("BD_BATCH_KERNEL", "streamk")
     cases = make_cases([(200, 1280, 3), (64, 384, 8), (130, 2048, 1)], seed0=300, mode=1)
-    with grid_override(grid):
-        ys, ws = run_batch(cases)
-    check_all(cases, ys, f"grid={grid}")
-    with grid_override(grid):
-        assert_reusable(cases, ys, ws, f"grid={grid}")
+    with bd.option(bd.BD_OPT_BATCH_KERNEL, 2):
+        with grid_override(grid):
+            ys, ws = run_batch(cases)
+        check_all(cases, ys, f"grid={grid}")
+        with grid_override(grid):
+            assert_reusable(cases, ys, ws, f"grid={grid}")
 
 
 @pytest.mark.parametrize("shape", [(200, 1280, 3), (4096, 4096, 16), (65, 128, 1), (1000, 8192, 9)])
-def test_single_linear_launch(shape, monkeypatch):
-    """A batch of one runs as bd_linear unless BD_BATCH_SINGLE=1 keeps it on the batched kernel."""
-    monkeypatch.setenv("BD_BATCH_SINGLE", "1")
+def test_single_linear_launch(shape):
+    """A batch of one runs as bd_linear unless BD_OPT_BATCH_SINGLE keeps it on the batched kernel."""
     cases = make_cases([shape], seed0=350, mode=1)
-    ys, ws = run_batch(cases)
-    check_all(cases, ys, f"single {shape}")
-    assert_reusable(cases, ys, ws, f"single {shape}")
+    with bd.option(bd.BD_OPT_BATCH_SINGLE, 1):
+        ys, ws = run_batch(cases)
+        check_all(cases, ys, f"single {shape}")
+        assert_reusable(cases, ys, ws, f"single {shape}")
 
 
 def test_deterministic_and_equal_across_repeats(batch_kernel):
