@@ -9,11 +9,16 @@ in HBM when the timed region starts; each phase is captured once as a CUDA
 graph and replayed, so host launch overhead is not timed, and CUDA events on
 the replay stream bracket every phase (they give the per-kernel roofline).
 
-The default workload is the Llama-7B-style layer at decode sizes (q/k/v/o
-4096x4096, gate/up 11008x4096, down 4096x11008; m = 1, 4, 16).  Its inputs
-(about 1.2 GB of W_base + W_ft + packed bits) are larger than L2, and the step
-order separates the two uses of any matrix by more than 250 MB of other
-traffic, so kernels read from HBM.
+The default workload is the 32-layer Llama-3-8B-shape stack (q 4096x4096, k/v
+1024x4096, o 4096x4096, gate/up 14336x4096, down 4096x14336 per layer): the
+compression of its 224 matrices, the fused linear of each at m = 1 (decode)
+and m = 2048 (prefill), the stack's multi-tenant decode (64 tokens over 14
+resident variants of the same base) and the 14-variant batch over one
+8192x8192 base (its compressions, 64 decode tokens, 2048 Zipf prefill tokens).
+`value` is the decode phase's fused-linear GB/s (algorithmic bytes over that
+phase's CUDA-event time); `prefill` gives the m = 2048 phase in TFLOP/s with its
+own roofline and CPU baseline.  Every input is far larger than L2 (14 GB of
+base weights per pass over the stack), so kernels read from HBM.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle on
@@ -156,6 +161,10 @@ class Phase:
         self.weight_prefetch = weight_prefetch
         self.graph = None
 
+    @property
+    def unit(self):
+        return "GB/s" if self.bound == "hbm" else "TFLOP/s"
+
     def run(self):
         for c in self.calls:
             c()
@@ -276,7 +285,7 @@ class LayerWorkload(Workload):
     Used for the Llama-7B layer at decode sizes (the default), the 70B-shape
     prefill linears and the Llama-3-8B-shape stack (decode or prefill)."""
 
-    def __init__(self, bd, dev, cfg, ms, unit, name, layers=1, private_io=True, batch="layer"):
+    def __init__(self, bd, dev, cfg, ms, unit, name, layers=1, private_io=True, batch="layer", phase_per_m=False):
         self.cfg, self.metric_unit = cfg, unit
         mode = cfg["mode"]
         shapes = [(f"L{l}.{n}", a, b) for l in range(layers) for (n, a, b) in cfg["matrices"]]
@@ -292,7 +301,14 @@ class LayerWorkload(Workload):
             layer_groups(names, FUSED_GROUPS[:1]) if self.batch == "qkv" else [[i] for i in range(len(shapes))]
         self.batch_ws = None
         self.linear_plan = []  # (matrices the call needs, call) for the pipelined end-to-end step
-        for m in ms:
+        self.lins = []  # one linear phase per token count (phase_per_m), else one for all of ms
+        bound = "hbm" if unit == "GB/s" else "tensor"
+        for mi, m in enumerate(ms):
+            if phase_per_m and mi > 0:
+                self.lins.append(Phase(f"fused_linear_m{ms[mi - 1]}", calls, bytes_=nbytes, flops=flops,
+                                       launches=launches, bound="hbm" if ms[mi - 1] <= 16 else "tensor",
+                                       weight_prefetch=WEIGHT_PREFETCH))
+                calls, nbytes, flops, launches = [], 0.0, 0.0, 0
             for grp in groups:
                 probs = []
                 for j, i in enumerate(grp):
@@ -323,10 +339,14 @@ class LayerWorkload(Workload):
                                  bd.bd_linear(x, wb, bits, alpha, mode, y))
                     launches += 1
                 self.linear_plan.append((set(grp), calls[-1]))
-        bound = "hbm" if unit == "GB/s" else "tensor"
-        self.lin = Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=launches, bound=bound,
-                         weight_prefetch=WEIGHT_PREFETCH)
-        self.phases = [self.comp, self.lin]
+        if phase_per_m:
+            self.lins.append(Phase(f"fused_linear_m{ms[-1]}", calls, bytes_=nbytes, flops=flops, launches=launches,
+                                   bound="hbm" if ms[-1] <= 16 else "tensor", weight_prefetch=WEIGHT_PREFETCH))
+        else:
+            self.lins.append(Phase("fused_linear", calls, bytes_=nbytes, flops=flops, launches=launches, bound=bound,
+                                   weight_prefetch=WEIGHT_PREFETCH))
+        self.lin = self.lins[0]
+        self.phases = [self.comp] + self.lins
         self.dominant = self.lin
         # one compression call per matrix, for the pipelined end-to-end step
         self.compress_one = []
@@ -343,8 +363,10 @@ class LayerWorkload(Workload):
                        "compress_batch": COMPRESS_BATCH,
                        "l2": "inputs larger than L2 (consecutive uses of a matrix separated by >250 MB of traffic)"}
 
-    def oracle_sample(self, oracle, frac_rows: float):
-        """Bounded CPU sample of one step: the first `frac_rows` of the first layer's rows."""
+    def oracle_sample(self, oracle, frac_rows: float, ms=None, compress=True):
+        """Bounded CPU sample of one step: the first `frac_rows` of the first layer's rows
+        (compression unless `compress` is false, then the fused linear at each m of `ms`,
+        default every m of the step, in the unit of that m's phase)."""
         cfg = self.cfg
         mode = cfg["mode"]
         first_layer = len(cfg["matrices"])
@@ -352,7 +374,8 @@ class LayerWorkload(Workload):
         for i, (wb, wf) in enumerate(self.mats[:first_layer]):
             n = max(8, int(wb.shape[0] * frac_rows))
             host.append((synth.as_u16(wb[:n]), synth.as_u16(wf[:n])))
-        ms = sorted({k[0] for k in self.xs})
+        ms = sorted({k[0] for k in self.xs}) if ms is None else sorted(ms)
+        unit = self.metric_unit if len(ms) > 1 else ("GB/s" if ms[0] <= 16 else "TFLOP/s")
         tok_cap = 64  # at most the first 64 tokens of each batch (prefill batches are thousands)
         xs = {}
         for m in ms:
@@ -360,21 +383,28 @@ class LayerWorkload(Workload):
                 key = (m, i) if (m, i) in self.xs else (m, n_in)
                 xs[(m, i)] = synth.as_u16(self.xs[key][:tok_cap])
 
+        # without the compression in the sample, its bits and alpha are made once outside it
+        pre = None if compress else [oracle.compress(wb, wf, mode)[:2] for (wb, wf) in host]
+
         def run():
             nbytes, flops = 0.0, 0.0
             packed = []
             for (wb, wf) in host:
-                bits, a32, _ = oracle.compress(wb, wf, mode)
-                packed.append((bits, a32))
-                nbytes += 4.0 * wb.size + wb.size / 8 + 4.0
+                if pre is None:
+                    bits, a32, _ = oracle.compress(wb, wf, mode)
+                    packed.append((bits, a32))
+                    nbytes += 4.0 * wb.size + wb.size / 8 + 4.0
+            if pre is not None:
+                packed = pre
             for (m, i), x in xs.items():
                 wb = host[i][0]
                 bits, a32 = packed[i]
                 oracle.linear(x, wb, bits, a32, mode)
                 nbytes += decode_bytes(x.shape[0], wb.shape[0], wb.shape[1], mode)
                 flops += 2.0 * x.shape[0] * wb.shape[0] * wb.shape[1]
-            return nbytes if self.metric_unit == "GB/s" else flops / 1e3
-        desc = (f"first layer, each matrix's first {frac_rows:.4g} of rows: compression + fused linear "
+            return nbytes if unit == "GB/s" else flops / 1e3
+        desc = (f"first layer, each matrix's first {frac_rows:.4g} of rows: "
+                + ("compression + " if compress else "") + "fused linear "
                 f"at m={','.join(str(min(m, tok_cap)) for m in ms)}"
                 + (" (first tokens of each batch)" if max(ms) > tok_cap else ""))
         return run, desc
@@ -382,13 +412,13 @@ class LayerWorkload(Workload):
 
 class GroupedWorkload(Workload):
     """14 variants over one 8192x8192 base: compress every variant, then one
-    multi-tenant linear (64 decode tokens with uniform ids, or 2048 prefill
-    tokens in Zipf(1.1) segments)."""
+    multi-tenant linear per kind -- 64 decode tokens with uniform ids, and/or
+    2048 prefill tokens in Zipf(1.1) segments."""
 
-    def __init__(self, bd, dev, kind):
+    def __init__(self, bd, dev, kinds=("decode",)):
         c = workloads.GROUPED_14
-        self.cfg, self.kind = c, kind
-        self.metric_unit = "GB/s" if kind == "decode" else "TFLOP/s"
+        self.cfg, self.kinds = c, tuple(kinds)
+        self.metric_unit = "GB/s" if self.kinds[0] == "decode" else "TFLOP/s"
         n_out, n_in, nv = c["n_out"], c["n_in"], c["n_variants"]
         g = synth.generator(c["seed"], dev)
         self.w_base = synth.bf16_normal((n_out, n_in), c["sigma"], g, dev)
@@ -399,39 +429,51 @@ class GroupedWorkload(Workload):
             del d
         self.mats = [(self.w_base, wf) for wf in self.fts]
         self.comp, self.packed = compress_phase(bd, self.mats, c["mode"], dev)
-        m = c["decode_m"] if kind == "decode" else c["prefill_m"]
-        ids = synth.uniform_ids(m, nv, c["seed"]) if kind == "decode" else synth.zipf_ids(m, nv, c["zipf_s"], c["seed"])
-        self.ids_h = ids
-        self.ids = torch.from_numpy(ids).to(dev)
-        self.x = synth.activations(m, n_in, c["seed"] + 1, dev)
-        self.y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
-        self.ws = torch.empty((bd.bd_linear_grouped_workspace_size(m, nv, n_out, n_in),), dtype=torch.uint8, device=dev)
         bits_v = [b for b, _ in self.packed]
         alpha_v = [a for _, a in self.packed]
         modes = [c["mode"]] * nv
-        call = lambda: bd.bd_linear_grouped(self.x, self.ids, self.w_base, bits_v, alpha_v, modes, self.y, self.ws)
-        active = len(set(ids.tolist()))
-        nbytes = 2.0 * n_out * n_in + active * n_out * n_in / 8 + 4.0 * nv + 2.0 * m * n_in + 2.0 * m * n_out
-        flops = 2.0 * m * n_out * n_in
-        bound = "hbm" if kind == "decode" else "tensor"
-        # the sort and gather kernels are tiny; the launch count is the library's whole call
-        self.lin = Phase("grouped_linear", [call], bytes_=nbytes, flops=flops, launches=3, bound=bound)
-        self.phases = [self.comp, self.lin]
+        self.lins, self.io, self.ids_h = [], [], {}
+        for kind in self.kinds:
+            m = c["decode_m"] if kind == "decode" else c["prefill_m"]
+            ids = synth.uniform_ids(m, nv, c["seed"]) if kind == "decode" else \
+                synth.zipf_ids(m, nv, c["zipf_s"], c["seed"])
+            self.ids_h[kind] = ids
+            ids_d = torch.from_numpy(ids).to(dev)
+            x = synth.activations(m, n_in, c["seed"] + 1, dev)
+            y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
+            ws = torch.empty((bd.bd_linear_grouped_workspace_size(m, nv, n_out, n_in),), dtype=torch.uint8,
+                             device=dev)
+            call = lambda x=x, ids_d=ids_d, y=y, ws=ws: bd.bd_linear_grouped(x, ids_d, self.w_base, bits_v, alpha_v,
+                                                                             modes, y, ws)
+            active = len(set(ids.tolist()))
+            nbytes = 2.0 * n_out * n_in + active * n_out * n_in / 8 + 4.0 * nv + 2.0 * m * n_in + 2.0 * m * n_out
+            flops = 2.0 * m * n_out * n_in
+            # the sort and gather kernels are tiny; the launch count is the library's whole call
+            self.lins.append(Phase(f"grouped_linear_{kind}", [call], bytes_=nbytes, flops=flops, launches=3,
+                                   bound="hbm" if kind == "decode" else "tensor"))
+            self.io.append(([x, ids_d], [y]))
+        self.lin = self.lins[0]
+        self.phases = [self.comp] + self.lins
         self.dominant = self.lin
-        self.h2d_tensors = list(self.fts) + [self.x, self.ids]
-        self.d2h_tensors = [self.y] + [a for (_, a) in self.packed]
-        self.config = {"workload": f"grouped_14_variants_8192_{kind}", "variants": nv, "tokens": m,
-                       "ids": "uniform" if kind == "decode" else "zipf(1.1) segments, shuffled",
-                       "active_variants": active, "alpha": "scalar per variant",
+        self.h2d_tensors = list(self.fts) + [t for ins, _ in self.io for t in ins]
+        self.d2h_tensors = [t for _, outs in self.io for t in outs] + [a for (_, a) in self.packed]
+        k = self.kinds[0]
+        self.config = {"workload": f"grouped_14_variants_8192_{k}", "variants": nv,
+                       "tokens": c["decode_m"] if k == "decode" else c["prefill_m"],
+                       "ids": "uniform" if k == "decode" else "zipf(1.1) segments, shuffled",
+                       "active_variants": len(set(self.ids_h[k].tolist())), "alpha": "scalar per variant",
                        "l2": "inputs larger than L2 (14 W_ft of 128 MB each are compressed every step)"}
 
-    def oracle_sample(self, oracle, frac_rows: float):
+    def oracle_sample(self, oracle, frac_rows: float, kind=None):
         c = self.cfg
+        kind = kind or self.kinds[0]
         n = max(8, int(c["n_out"] * frac_rows))
         wb = synth.as_u16(self.w_base[:n])
         fts = [synth.as_u16(wf[:n]) for wf in self.fts]
-        x = synth.as_u16(self.x)
+        x = synth.as_u16(self.io[self.kinds.index(kind)][0][0])
+        ids = self.ids_h[kind]
         modes = np.zeros(len(fts), np.int32)
+        unit = "GB/s" if kind == "decode" else "TFLOP/s"
 
         def run():
             bits, alphas = [], []
@@ -440,12 +482,38 @@ class GroupedWorkload(Workload):
                 b, a, _ = oracle.compress(wb, wf, 0)
                 bits.append(b), alphas.append(a)
                 nbytes += 4.0 * wb.size + wb.size / 8
-            oracle.linear_grouped(x, self.ids_h, wb, bits, alphas, modes)
+            oracle.linear_grouped(x, ids, wb, bits, alphas, modes)
             m = x.shape[0]
-            if self.metric_unit == "GB/s":
+            if unit == "GB/s":
                 return nbytes + 2.0 * wb.size + len(fts) * wb.size / 8 + 2.0 * m * wb.shape[1] + 2.0 * m * n
             return 2.0 * m * wb.size / 1e3
-        return run, f"first {frac_rows:.4g} of the rows: 14 compressions + the multi-tenant linear"
+        return run, f"first {frac_rows:.4g} of the rows: 14 compressions + the multi-tenant linear ({kind})"
+
+
+def compress_variants(bd, dev, w_base, scales, seed, mode=0):
+    """Bits and alpha of one fine-tuned variant per scale of `scales` over `w_base`: W_ft =
+    bf16(fp32(W_base) + Laplace(0, b)) drawn on the device and compressed by the library, in
+    bd_compress_batch calls of up to 8 variants; the W_ft are freed afterwards."""
+    n_out, n_in = w_base.shape
+    out = []
+    for v0 in range(0, len(scales), 8):
+        fts, descs_in = [], []
+        for v in range(v0, min(len(scales), v0 + 8)):
+            g = synth.generator(seed * 131 + v, dev)
+            d = synth.laplace_f32((n_out, n_in), scales[v], g, dev)
+            wf = d.add_(w_base.float()).to(torch.bfloat16)
+            del d
+            bits = torch.empty((n_out, n_in // 8), dtype=torch.uint8, device=dev)
+            alpha = torch.empty((n_out if mode == 1 else 1,), dtype=torch.float32, device=dev)
+            fts.append(wf)
+            descs_in.append((w_base, wf, mode, bits, alpha))
+            out.append((bits, alpha))
+        descs = bd.compress_descs(descs_in)
+        ws = torch.empty((max(256, bd.bd_compress_batch_workspace_size(descs)),), dtype=torch.uint8, device=dev)
+        bd.bd_compress_batch(descs, ws)
+        torch.cuda.synchronize()
+        del fts
+    return out
 
 
 class GroupedStackWorkload(Workload):
@@ -453,12 +521,13 @@ class GroupedStackWorkload(Workload):
     Llama-3-8B-shape stack as one multi-tenant call, 64 tokens whose ids are
     uniform over 14 variants, all 224 calls replayed as one CUDA graph.
 
-    The 14 variants' deltas are resident (as behind the delta cache); their sign
-    bits are seeded random bytes (a Laplace delta's signs are balanced) and their
-    alpha the variant's scale, so no fine-tuned weights have to be held (14 x 14 GB);
-    the compression of the stack is measured by the llama3_8b_stack_* workloads."""
+    Each variant's delta of each matrix is compressed by the library from a
+    fine-tuned W_ft = bf16(W_base + Laplace(0, b_v)) drawn on the device (b_v the
+    14 evenly spaced scales of the 14-variant workload) and resident afterwards, as
+    behind the delta cache; the W_ft are not kept (14 x 14 GB).  `bases` shares
+    the W_base matrices of another workload (one resident base for every tenant)."""
 
-    def __init__(self, bd, dev):
+    def __init__(self, bd, dev, bases=None):
         c = workloads.LLAMA3_8B_STACK
         g14 = workloads.GROUPED_14
         self.cfg = c
@@ -474,11 +543,14 @@ class GroupedStackWorkload(Workload):
         calls, nbytes, flops = [], 0.0, 0.0
         self.first = None
         for i, (n_out, n_in) in enumerate(shapes):
-            gen = synth.generator(workloads.matrix_seed(c["seed"], 1000 + i), dev)
-            wb = synth.bf16_normal((n_out, n_in), c["sigma"], gen, dev)
-            bits_v = [torch.randint(0, 256, (n_out, n_in // 8), generator=gen, device=dev, dtype=torch.uint8)
-                      for _ in range(nv)]
-            alpha_v = [torch.full((1,), float(b), dtype=torch.float32, device=dev) for b in scales]
+            if bases is not None:
+                wb = bases[i]
+            else:
+                gen = synth.generator(workloads.matrix_seed(c["seed"], 1000 + i), dev)
+                wb = synth.bf16_normal((n_out, n_in), c["sigma"], gen, dev)
+            packed = compress_variants(bd, dev, wb, scales, workloads.matrix_seed(c["seed"], 5000 + i))
+            bits_v = [b for b, _ in packed]
+            alpha_v = [a for _, a in packed]
             if n_in not in self.xs:
                 self.xs[n_in] = synth.activations(m, n_in, 20_000 + n_in, dev)
                 self.wss[n_in] = {}
@@ -503,7 +575,7 @@ class GroupedStackWorkload(Workload):
         self.config = {"workload": "llama3_8b_stack_grouped14_decode", "layers": c["layers"],
                        "matrices": sorted({f"{a}x{b}" for _, a, b in c["matrices"]}), "variants": nv, "tokens": m,
                        "ids": "uniform", "active_variants": active,
-                       "deltas": "resident; seeded random sign bits, alpha = the variant's Laplace scale",
+                       "deltas": "resident; each compressed by bd_compress_batch from W_base + Laplace(0, b_v)",
                        "l2": "inputs larger than L2 (14 GB of base weights and 12 GB of bits per step)"}
 
     def oracle_sample(self, oracle, frac_rows: float):
@@ -522,6 +594,62 @@ class GroupedStackWorkload(Workload):
         return run, f"first {frac_rows:.4g} of the rows of the first matrix: the multi-tenant linear"
 
 
+def renamed(phase, name):
+    phase.name = name
+    return phase
+
+
+class ServingWorkload(Workload):
+    """The default step: the whole hot path over the 32-layer Llama-3-8B-shape stack.
+
+    Phases, each one CUDA graph: compression of the 224 matrices; the fused linear of
+    every matrix at m = 1 (decode) and at m = 2048 (prefill); the stack's serving decode
+    with 64 tokens over 14 resident variants on the same base (one multi-tenant call per
+    matrix); and the 14-variant batch over one 8192x8192 base -- its 14 compressions, 64
+    decode tokens with uniform ids and 2048 prefill tokens in Zipf(1.1) segments.
+    `value` is the fused-linear GB/s of the decode phase (its algorithmic bytes over its
+    own CUDA-event time); the prefill phase reports TFLOP/s beside it.  With
+    `reference`, only the first layer is built (the CPU arm samples it)."""
+
+    metric_unit = "GB/s"
+
+    def __init__(self, bd, dev, reference=False):
+        c = workloads.LLAMA3_8B_STACK
+        self.cfg, self.bd = c, bd
+        self.stack = LayerWorkload(bd, dev, c, (1, 2048), "GB/s", "llama3_8b_stack",
+                                   layers=1 if reference else c["layers"], private_io=False, phase_per_m=True)
+        self.decode = renamed(self.stack.lins[0], "fused_linear_decode")
+        self.prefill = renamed(self.stack.lins[1], "fused_linear_prefill")
+        self.phases = [self.stack.comp, self.decode, self.prefill]
+        self.tenants = self.g14 = None
+        if not reference:
+            self.tenants = GroupedStackWorkload(bd, dev, bases=[wb for wb, _ in self.stack.mats])
+            self.g14 = GroupedWorkload(bd, dev, kinds=("decode", "prefill"))
+            self.phases += [renamed(self.tenants.lin, "multi_tenant_stack_decode"),
+                            renamed(self.g14.comp, "compress_14_variants"),
+                            renamed(self.g14.lins[0], "multi_tenant_decode"),
+                            renamed(self.g14.lins[1], "multi_tenant_prefill")]
+        self.headline, self.secondary = self.decode, self.prefill
+        self.dominant = self.decode
+        g14 = workloads.GROUPED_14
+        self.config = {"workload": "llama3_8b_stack", "layers": c["layers"],
+                       "matrices": sorted({f"{a}x{b}" for _, a, b in c["matrices"]}),
+                       "matrix_count": c["layers"] * len(c["matrices"]), "tokens": {"decode": 1, "prefill": 2048},
+                       "alpha": "scalar", "dtype_in": "bf16 weights/activations",
+                       "value": "fused-linear GB/s of the m = 1 phase (its algorithmic bytes / its CUDA-event time)",
+                       "weight_prefetch": WEIGHT_PREFETCH, "linear_batch": self.stack.batch,
+                       "compress_batch": COMPRESS_BATCH,
+                       "multi_tenant": {"stack_decode": f"{g14['decode_m']} tokens, uniform ids over "
+                                                       f"{g14['n_variants']} variants, every stack matrix",
+                                        "batch_8192": f"{g14['n_variants']} variants over one 8192x8192 base: "
+                                                      f"{g14['decode_m']} decode tokens (uniform ids), "
+                                                      f"{g14['prefill_m']} prefill tokens (Zipf(1.1) segments)"},
+                       "l2": "inputs larger than L2 (14 GB of base weights per pass over the stack)"}
+
+    def oracle_sample(self, oracle, frac_rows: float, phase="decode"):
+        return self.stack.oracle_sample(oracle, frac_rows, ms=(1,) if phase == "decode" else (2048,), compress=False)
+
+
 WORKLOADS = {
     "llama7b_layer_decode": lambda bd, dev: LayerWorkload(
         bd, dev, workloads.LLAMA7B_LAYER, workloads.LLAMA7B_LAYER["ms"], "GB/s", "llama7b_layer_decode",
@@ -529,8 +657,9 @@ WORKLOADS = {
     "llama70b_linears_prefill": lambda bd, dev: LayerWorkload(
         bd, dev, workloads.LLAMA70B_PREFILL, workloads.LLAMA70B_PREFILL["ms"], "TFLOP/s", "llama70b_linears_prefill",
         private_io=False),
-    "grouped14_decode": lambda bd, dev: GroupedWorkload(bd, dev, "decode"),
-    "grouped14_prefill": lambda bd, dev: GroupedWorkload(bd, dev, "prefill"),
+    "grouped14_decode": lambda bd, dev: GroupedWorkload(bd, dev, ("decode",)),
+    "grouped14_prefill": lambda bd, dev: GroupedWorkload(bd, dev, ("prefill",)),
+    "llama3_8b_stack": lambda bd, dev: ServingWorkload(bd, dev),
     "llama3_8b_stack_decode": lambda bd, dev: LayerWorkload(
         bd, dev, workloads.LLAMA3_8B_STACK, (1,), "GB/s", "llama3_8b_stack_decode",
         layers=workloads.LLAMA3_8B_STACK["layers"], private_io=False),
@@ -596,18 +725,27 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status after timing: {bd.bd_status_string(status)}")
 
     t_max = max_over_ranks(ws, total_ms)
-    value = aggregate_value(ws, args.steps, wl.step_work(), t_max)
+    head = getattr(wl, "headline", None)
+    if head is not None:
+        # value: the headline phase's work over its own time (summed over the timed steps)
+        h_ms = max_over_ranks(ws, phase_ms[wl.phases.index(head)])
+        value = aggregate_value(ws, args.steps, head.bytes if head.bound == "hbm" else head.flops / 1e3, h_ms)
+    else:
+        value = aggregate_value(ws, args.steps, wl.step_work(), t_max)
+
+    def roofline(p):
+        t = phase_ms[wl.phases.index(p)] * 1e-3 / (args.steps * p.launches)  # average launch
+        if p.bound == "hbm":
+            achieved, peak, unit = p.bytes / p.launches / t / 1e9, peaks["hbm"], "GB/s"
+        else:
+            achieved, peak, unit = p.flops / p.launches / t / 1e12, peaks["bf16"], "TFLOP/s"
+        r = {"bound": p.bound, "kernel": p.name, "achieved": achieved, "peak": peak, "unit": unit,
+             "frac": achieved / peak, "peak_source": peaks["source"], "traffic": lookup_traffic(args.workload, p)}
+        if p.bound == "tensor":
+            r["frac_of_sustained"] = achieved / peaks["bf16_sustained"]
+        return r
 
     dom = wl.dominant
-    dom_idx = wl.phases.index(dom)
-    dom_launch_s = phase_ms[dom_idx] * 1e-3 / (args.steps * dom.launches)
-    if dom.bound == "hbm":
-        achieved = dom.bytes / dom.launches / dom_launch_s / 1e9
-        peak, unit = peaks["hbm"], "GB/s"
-    else:
-        achieved = dom.flops / dom.launches / dom_launch_s / 1e12
-        peak, unit = peaks["bf16"], "TFLOP/s"
-    traffic = lookup_traffic(args.workload, dom)
     breakdown = {}
     for j, p in enumerate(wl.phases):
         t = phase_ms[j] * 1e-3 / args.steps
@@ -620,50 +758,106 @@ def run_ours(args, ws, rank, local):
                                  "frac_of_measured_bf16": p.flops / t / 1e12 / peaks["bf16"],
                                  "launches": p.launches}
 
-    e2e = run_e2e(args, wl, stream, ws) if not args.no_e2e else None
+    if args.no_e2e:
+        e2e = None
+    elif isinstance(wl, ServingWorkload):
+        e2e = run_e2e_serving(args, wl, stream, ws)
+    else:
+        e2e = run_e2e(args, wl, stream, ws)
     cpu = cpu_baseline(wl, args) if (rank == 0 and not args.no_cpu) else None
 
     line = {
         "metric": "BitDelta fused linear GB/s (decode) & TFLOP/s (prefill), % of roofline",
-        "value": value, "unit": wl.metric_unit, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "value": value, "unit": head.unit if head is not None else wl.metric_unit, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded; N(0,sigma) bf16 base, Laplace deltas, N(0,1) activations)",
         "config": dict(wl.config, parallelism=f"replicas{ws}" if ws > 1 else "single"),
-        "roofline": {"bound": dom.bound, "kernel": dom.name, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "peak_source": peaks["source"], "traffic": traffic,
-                     **({"frac_of_sustained": achieved / peaks["bf16_sustained"]} if dom.bound == "tensor" else {})},
+        "roofline": roofline(dom),
         "breakdown": breakdown,
         "e2e": e2e,
         "gpu_launches": args.steps * sum(p.launches for p in wl.phases),
         "clocks": clock_info,
         "cpu_baseline": cpu,
     }
+    sec = getattr(wl, "secondary", None)
+    if sec is not None:
+        s_ms = max_over_ranks(ws, phase_ms[wl.phases.index(sec)])
+        sv = aggregate_value(ws, args.steps, sec.bytes if sec.bound == "hbm" else sec.flops / 1e3, s_ms)
+        line["prefill"] = {"value": sv, "unit": sec.unit, "tokens": 2048, "roofline": roofline(sec),
+                           "e2e": (e2e or {}).get("segments", {}).get(sec.name),
+                           "cpu_baseline": cpu_baseline(wl, args, phase="prefill")
+                           if (rank == 0 and not args.no_cpu) else None}
+    if isinstance(wl, ServingWorkload):
+        line["multi_tenant"] = {p.name: roofline(p) for p in wl.phases
+                                if p.name.startswith("multi_tenant")}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-KERNEL_SOURCES = {"hbm": ("decode_tma.cu", "decode_batch.cu", "decode_stage.cuh", "api.cu"), "tensor": ("prefill.cu",)}
+# Sources whose change invalidates a stored traffic figure, by phase bound.
+KERNEL_SOURCES = {"hbm": ("decode_tma.cu", "decode_batch.cu", "decode_stage.cuh", "grouped_decode.cu", "grouped.cu",
+                          "compress.cu", "api.cu"),
+                  "tensor": ("prefill.cu", "grouped.cu", "api.cu")}
+
+
+def traffic_path(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+
+
+def sources_sha1(bound: str) -> str:
+    import hashlib
+    h = hashlib.sha1()
+    for name in KERNEL_SOURCES[bound]:
+        with open(os.path.join(ROOT, "bit_delta_tenant_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def lookup_traffic(workload: str, phase):
-    """DRAM bytes per launch of the dominant phase's kernels from the committed ncu summary
-    profiles/traffic_<workload>.md, if their sources are unchanged since the capture (SHA-1
-    over the sources of KERNEL_SOURCES, in that order)."""
-    import hashlib
-    import re
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.md")
+    """DRAM bytes per launch of `phase` from profiles/traffic_<workload>.json (written by
+    --ingest-traffic from a one-kernel ncu capture), if the kernel sources are unchanged since."""
     try:
-        text = open(path).read()
-        h = hashlib.sha1()
-        for name in KERNEL_SOURCES[phase.bound]:
-            h.update(open(os.path.join(ROOT, "bit_delta_tenant_gb300", "csrc", name), "rb").read())
-        digest = h.hexdigest()
+        with open(traffic_path(workload)) as f:
+            rec = json.load(f).get(phase.name)
+        if rec is None or rec.get("source_sha1") != sources_sha1(phase.bound):
+            return None
+        return float(rec["traffic_per_launch_bytes"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def ingest_traffic(args):
+    """--ingest-traffic CSV --phase NAME: the mean dram__bytes_read.sum + dram__bytes_write.sum per
+    launch of an ncu --csv capture (one kernel, a few launches) into profiles/traffic_<workload>.json."""
+    import csv
+    per = {}
+    with open(args.ingest_traffic, newline="") as f:
+        rows = [r for r in csv.reader(f) if r]
+    hdr = next(i for i, r in enumerate(rows) if "Metric Name" in r)
+    cols = rows[hdr]
+    ci, cm, cv, cu = (cols.index(k) for k in ("ID", "Metric Name", "Metric Value", "Metric Unit"))
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9}
+    for r in rows[hdr + 1:]:
+        if len(r) <= max(ci, cm, cv, cu) or r[cm] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        per[r[ci]] = per.get(r[ci], 0.0) + float(r[cv].replace(",", "")) * scale.get(r[cu], 1.0)
+    if not per:
+        raise SystemExit("no dram__bytes_(read|write).sum rows in the capture")
+    bound = "tensor" if args.phase in ("fused_linear_prefill", "multi_tenant_prefill") else "hbm"
+    path = traffic_path(args.workload)
+    try:
+        with open(path) as f:
+            data = json.load(f)
     except OSError:
-        return None
-    m = re.search(r"traffic_per_launch_bytes:\s*([0-9.eE+]+)\s+source_sha1:\s*([0-9a-f]+)", text)
-    if not m or m.group(2) != digest:
-        return None
-    return float(m.group(1))
+        data = {}
+    data[args.phase] = {"traffic_per_launch_bytes": sum(per.values()) / len(per), "launches_captured": len(per),
+                        "source_sha1": sources_sha1(bound), "sources": list(KERNEL_SOURCES[bound]),
+                        "command": args.ingest_command or ""}
+    with open(path, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({args.phase: data[args.phase]}))
 
 
 def pipelined_step(wl, h2d, d2h, stream, copy_stream):
@@ -774,6 +968,127 @@ def run_e2e(args, wl, stream, ws):
             "copies": "overlapped with the compressions and linears, and with the previous step" if pipelined else "before the step"}
 
 
+def run_e2e_serving(args, wl, stream, ws):
+    """The default step end to end through the C ABI with host buffers, in segments whose
+    CUDA-event times each include their own copies: (1) every W_ft from pinned host memory,
+    each matrix compressed as soon as its copy has landed (copies on a second stream), alpha
+    back; (2) the decode activations up, the m = 1 linears, y back; (3) the same at m = 2048;
+    (4) the multi-tenant phases, each with its activations and ids up and y back.  W_base and
+    the variants' packed deltas stay resident, as on the page.  `value` is the decode
+    segment's fused-linear GB/s.  After timing, every output of the last step is checked bit
+    for bit against a replay of the device-resident graphs."""
+    st = wl.stack
+    copy_stream = torch.cuda.Stream()
+    pin = lambda t: torch.empty_like(t, device="cpu").pin_memory()
+
+    def host_of(ts):
+        out = []
+        for t in ts:
+            h = pin(t)
+            h.copy_(t)
+            out.append((h, t))
+        return out
+    mats = list(st.mats) + (list(wl.g14.mats) if wl.g14 is not None else [])
+    comp_one = list(st.compress_one)
+    if wl.g14 is not None:
+        for (wb, wf), (bits, alpha) in zip(wl.g14.mats, wl.g14.packed):
+            descs = wl.bd.compress_descs([(wb, wf, wl.g14.cfg["mode"], bits, alpha)])
+            wsb = torch.empty((max(256, wl.bd.bd_compress_batch_workspace_size(descs)),), dtype=torch.uint8,
+                              device=wb.device)
+            comp_one.append(lambda descs=descs, wsb=wsb: wl.bd.bd_compress_batch(descs, wsb))
+    wft_h = host_of([wf for _, wf in mats])
+    alphas = [a for _, a in st.packed] + ([a for _, a in wl.g14.packed] if wl.g14 is not None else [])
+    alpha_h = [(pin(a), a) for a in alphas]
+    segs = []  # (name, phase or None, h2d pairs, d2h pairs)
+    xs_of = {m: [t for (mm, _), t in st.xs.items() if mm == m] for m in (1, 2048)}
+    ys_of = {m: [t for (mm, _, _), t in st.ys.items() if mm == m] for m in (1, 2048)}
+    segs.append(("fused_linear_decode", wl.decode, host_of(xs_of[1]), [(pin(t), t) for t in ys_of[1]]))
+    segs.append(("fused_linear_prefill", wl.prefill, host_of(xs_of[2048]), [(pin(t), t) for t in ys_of[2048]]))
+    if wl.tenants is not None:
+        tn = wl.tenants
+        segs.append(("multi_tenant_stack_decode", tn.lin, host_of(list(tn.xs.values()) + [tn.ids]),
+                     [(pin(t), t) for t in tn.ys.values()]))
+        for ph, (ins, outs) in zip(wl.g14.lins, wl.g14.io):
+            segs.append((ph.name, ph, host_of(ins), [(pin(t), t) for t in outs]))
+    n = len(mats)
+    landed = [torch.cuda.Event() for _ in range(n)]
+    ev = []
+
+    def one(record):
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(len(segs) + 2)] if record else None
+        with torch.cuda.stream(stream):
+            if record:
+                marks[0].record(stream)
+            copy_stream.wait_stream(stream)  # no copy of this step starts before its first mark
+            with torch.cuda.stream(copy_stream):
+                for i in range(n):
+                    wft_h[i][1].copy_(wft_h[i][0], non_blocking=True)
+                    landed[i].record(copy_stream)
+            for i in range(n):
+                stream.wait_event(landed[i])
+                comp_one[i]()
+            for h, d in alpha_h:
+                h.copy_(d, non_blocking=True)
+            if record:
+                marks[1].record(stream)
+            for k, (_, ph, up, down) in enumerate(segs):
+                for h, d in up:
+                    d.copy_(h, non_blocking=True)
+                ph.replay()
+                for h, d in down:
+                    h.copy_(d, non_blocking=True)
+                if record:
+                    marks[k + 2].record(stream)
+            stream.wait_stream(copy_stream)
+        if record:
+            ev.append(marks)
+
+    for _ in range(max(1, args.warmup)):
+        one(False)
+    torch.cuda.synchronize()
+    barrier(ws)
+    for _ in range(args.steps):
+        one(True)
+    torch.cuda.synchronize()
+    seg_ms = [0.0] * (len(segs) + 1)
+    for marks in ev:
+        for k in range(len(segs) + 1):
+            seg_ms[k] += marks[k].elapsed_time(marks[k + 1])
+    total = sum(ev[i][0].elapsed_time(ev[i][-1]) for i in range(len(ev)))
+    # outputs of the last step against the device-resident graphs
+    got = [h.clone() for h, _ in alpha_h] + [h.clone() for _, _, _, down in segs for h, _ in down]
+    with torch.cuda.stream(stream):
+        for p in wl.phases:
+            p.replay()
+    torch.cuda.synchronize()
+    ref = [d for _, d in alpha_h] + [d for _, _, _, down in segs for _, d in down]
+    for g, d in zip(got, ref):
+        if not torch.equal(g, d.cpu()):
+            raise RuntimeError("end-to-end step and device-resident step disagree")
+    steps = args.steps
+    bi = sum(h.numel() * h.element_size() for h, _ in wft_h) + \
+        sum(h.numel() * h.element_size() for _, _, up, _ in segs for h, _ in up)
+    bo = sum(h.numel() * h.element_size() for h, _ in alpha_h) + \
+        sum(h.numel() * h.element_size() for _, _, _, down in segs for h, _ in down)
+    comp_bytes = st.comp.bytes + (wl.g14.comp.bytes if wl.g14 is not None else 0.0)
+    segments = {"compress": {"ms_per_step": seg_ms[0] / steps, "unit": "GB/s",
+                             "value": ws * steps * comp_bytes / (max_over_ranks(ws, seg_ms[0]) * 1e-3) / 1e9,
+                             "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h, _ in wft_h),
+                             "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h, _ in alpha_h),
+                             "copies": "W_ft per matrix on a second stream, each compressed once landed"}}
+    for k, (name, ph, up, down) in enumerate(segs):
+        t = max_over_ranks(ws, seg_ms[k + 1])
+        work = ph.bytes if ph.bound == "hbm" else ph.flops / 1e3
+        segments[name] = {"ms_per_step": seg_ms[k + 1] / steps, "unit": ph.unit,
+                          "value": ws * steps * work / (t * 1e-3) / 1e9,
+                          "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h, _ in up),
+                          "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h, _ in down)}
+    dec = segments["fused_linear_decode"]
+    return {"value": dec["value"], "unit": "GB/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": total / steps, "value_segment": "fused_linear_decode (its activations up, y back)",
+            "segments": segments}
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -781,16 +1096,18 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, args, target_s: float = 12.0):
+def cpu_baseline(wl, args, target_s: float = 12.0, phase=None):
     import oracle
     oracle.build()
     frac = 1.0 / 64
-    run, _ = wl.oracle_sample(oracle, frac)
+    kw = {"phase": phase} if phase is not None else {}
+    unit = wl.metric_unit if phase is None else ("TFLOP/s" if phase == "prefill" else "GB/s")
+    run, _ = wl.oracle_sample(oracle, frac, **kw)
     t0 = time.perf_counter()
     run()
     t1 = time.perf_counter() - t0
     frac = min(1.0, frac * max(1.0, target_s / max(t1, 1e-3)))
-    run, desc = wl.oracle_sample(oracle, frac)
+    run, desc = wl.oracle_sample(oracle, frac, **kw)
     t0 = time.perf_counter()
     nbytes = run()
     dt = time.perf_counter() - t0
@@ -804,7 +1121,7 @@ def cpu_baseline(wl, args, target_s: float = 12.0):
         dt += time.perf_counter() - t0
         reps += more
         desc = desc.replace("each matrix's first 1 of rows", "every row of every matrix") + f", {reps} passes"
-    return {"value": nbytes / dt / 1e9, "unit": wl.metric_unit, "cores": cpu_cores(), "kind": "oracle",
+    return {"value": nbytes / dt / 1e9, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
             "sample": desc, "seconds": dt}
 
 
@@ -819,18 +1136,22 @@ def run_reference(args, ws, rank):
     oracle.build()
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     from bit_delta_tenant_gb300 import bitdelta as bd  # noqa: F401  (workload construction only)
-    wl = WORKLOADS[args.workload](_NoLib(), dev)
+    serving = args.workload == "llama3_8b_stack"
+    # the default step's CPU arm samples its first layer, so only that layer is built
+    wl = ServingWorkload(_NoLib(), dev, reference=True) if serving else WORKLOADS[args.workload](_NoLib(), dev)
+    kw = {"phase": "decode"} if serving else {}
+    unit = "GB/s" if serving else wl.metric_unit
     # Each step is the largest row sample (up to the whole step) that keeps the run near
     # REFERENCE_BUDGET_S: one 1/64 sample is timed first and scaled.
     frac = 1.0 / 64
-    run, desc = wl.oracle_sample(oracle, frac)
+    run, desc = wl.oracle_sample(oracle, frac, **kw)
     t0 = time.perf_counter()
     run()
     t_small = time.perf_counter() - t0
     budget_frac = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup) / max(t_small, 1e-4) * frac
     if budget_frac > frac:
         frac = min(1.0, budget_frac)
-        run, desc = wl.oracle_sample(oracle, frac)
+        run, desc = wl.oracle_sample(oracle, frac, **kw)
         if frac >= 1.0:
             desc = desc.replace("each matrix's first 1 of rows", "every row of every matrix")
     for _ in range(args.warmup):
@@ -842,12 +1163,17 @@ def run_reference(args, ws, rank):
     dt = time.perf_counter() - t0
     v = args.steps * nbytes / dt / 1e9
     line = {"impl": "reference", "metric": "BitDelta fused linear GB/s (decode) & TFLOP/s (prefill), % of roofline",
-            "value": v, "unit": wl.metric_unit, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "value": v, "unit": unit, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": wl.config,
-            "cpu_baseline": {"value": v, "unit": wl.metric_unit, "cores": cpu_cores(), "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
                              "sample": desc},
-            "e2e": {"value": v, "unit": wl.metric_unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if serving:
+        # the prefill half of the metric: the oracle's fused linear at m = 2048 (first 64 tokens)
+        line["prefill"] = {"cpu_baseline": cpu_baseline(wl, args, target_s=8.0, phase="prefill")}
+        line["prefill"]["value"] = line["prefill"]["cpu_baseline"]["value"]
+        line["prefill"]["unit"] = "TFLOP/s"
     print(json.dumps(line), flush=True)
 
 
@@ -1076,7 +1402,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama7b_layer_decode")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama3_8b_stack")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--weight-prefetch", type=int, choices=[0, 1], default=1,
@@ -1088,7 +1414,15 @@ def main():
                     help="compress through bd_compress_batch (8 matrices per call) or one bd_compress each")
     ap.add_argument("--kernel-case", default=None,
                     help="linear:N_OUTxN_IN:M[:path] or compress:N_OUTxN_IN[:mode] (one kernel, eager)")
+    ap.add_argument("--ingest-traffic", default=None,
+                    help="ncu --csv capture (dram__bytes_read.sum, dram__bytes_write.sum) to store as the "
+                         "traffic of --phase of --workload in profiles/traffic_<workload>.json")
+    ap.add_argument("--phase", default="fused_linear_decode")
+    ap.add_argument("--ingest-command", default=None, help="the command line of that capture, stored beside it")
     args = ap.parse_args()
+    if args.ingest_traffic:
+        ingest_traffic(args)
+        return
     global WEIGHT_PREFETCH, LINEAR_BATCH, COMPRESS_BATCH
     WEIGHT_PREFETCH = bool(args.weight_prefetch)
     LINEAR_BATCH = args.linear_batch
