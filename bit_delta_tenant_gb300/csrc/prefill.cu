@@ -17,8 +17,9 @@
 //               blocks (so two blocks are rebuilt at once): one thread per tile
 //               row, with the row's 8 packed bytes of the block (prefetched
 //               three of its blocks ahead); it rebuilds the row's eight 16-byte
-//               chunks of the swizzled W tile as bf16(fp32(W_base) + alpha_r*s)
-//               -- one chunk is exactly one packed byte.  After the K loop the
+//               chunks of the swizzled W tile as bf16(W_base + alpha_r*s), one
+//               bf16x2 add per pair with alpha_r rounded to bf16 -- one chunk is
+//               exactly one packed byte.  After the K loop the
 //               same warps are the epilogue (warp w reads TMEM lanes
 //               32*(w%4)..+31, the two groups splitting the token columns).
 //   warp 1      allocates TMEM (256 accumulator columns, plus 32 columns per
@@ -92,15 +93,20 @@ struct PrefillArgs {
     int32_t vmode[kMaxVariants];
 };
 
-// One bf16 pair of W_eff = bf16(fp32(W_base) + alpha * s): the sign bit of
-// -alpha is cleared where the packed bit is 1 (+alpha) and kept where it is 0.
+// One bf16 pair of W_eff = W_base + alpha_b * s, rounded once to bf16
+// (add.rn.bf16x2 adds exactly, then rounds to nearest even), with alpha_b =
+// alpha rounded to bf16.  The pair of signed scales is built from -alpha_b in
+// both halves: one multiply moves bit 2I of the packed byte to bit 15 and bit
+// 2I+1 to bit 31 (the two shifted copies never overlap), and the xor clears the
+// sign of -alpha_b where the bit is 1 (+alpha_b).  Three operations per pair
+// instead of widening to fp32 and packing back.
 template <int I>
-__device__ __forceinline__ uint32_t rebuild_pair(uint32_t w, uint32_t byte, uint32_t neg_alpha_bits) {
-    const uint32_t s_lo = ((byte << (31 - 2 * I)) & 0x80000000u) ^ neg_alpha_bits;
-    const uint32_t s_hi = ((byte << (30 - 2 * I)) & 0x80000000u) ^ neg_alpha_bits;
-    const float lo = bf16lo_to_f32(w) + __uint_as_float(s_lo);
-    const float hi = bf16hi_to_f32(w) + __uint_as_float(s_hi);
-    return pack_bf16x2(lo, hi);
+__device__ __forceinline__ uint32_t rebuild_pair(uint32_t w, uint32_t byte, uint32_t neg_alpha2) {
+    constexpr uint32_t mul = (1u << (15 - 2 * I)) + (1u << (30 - 2 * I));
+    const uint32_t s = ((byte * mul) & 0x80008000u) ^ neg_alpha2;
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(s));
+    return r;
 }
 
 __device__ __forceinline__ void give_up(volatile int *abort_flag, unsigned *status) {
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t row = static_cast<int64_t>(m0) + r;
         const bool row_ok = row < a.n_out;
         const float al = (row_ok && alpha != nullptr) ? (mode ? alpha[row] : alpha[0]) : 0.0f;  // none: base only
-        const uint32_t neg_al = __float_as_uint(-al);
+        const uint32_t neg_al = pack_bf16x2(-al, -al);  // -alpha_b in both halves
         const int64_t bpr = a.n_in / 8;
         const uint8_t *brow = bits != nullptr ? bits + (row_ok ? row : 0) * bpr : nullptr;
 
