@@ -291,6 +291,52 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
            | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
 
+// ---- CTA pairs (cta_group::2): one MMA over the tensor memory of two CTAs ------------
+// Tensor memory of a CTA pair: one warp of EACH CTA of the pair executes the
+// allocation (and later the deallocation) collectively; every tcgen05 operation
+// of a kernel that uses them takes .cta_group::2.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]^T over the pair: M = 256 rows, rows 0..127 in the
+// issuing (even) CTA's tensor memory and 128..255 in its peer's, at the same addresses
+// (A the same way); B's N rows are split in halves, the first N/2 in the issuing CTA's
+// shared memory and the rest in the peer's, at the same offset.
+__device__ __forceinline__ void tc_mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the mbarrier at offset `bar` in every CTA of `cta_mask` (cluster ranks)
+// when every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, given its shared::cluster address
+// (mapa_rank), with the default release at CTA scope.  What the arriving threads hand
+// over is ordered by the tensor-memory fences around the arrive and by the TMA
+// completion they observed, not by generic stores; a cluster-scope release here would
+// fence every arrival (measured: it stalled the pair kernel's rebuild warps on memory
+// barriers).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 // ---- legacy warp-level MMA (used by the HBM-streaming decode kernels) ---------------
 // D(16x8, f32) += A(16x16, bf16, row) * B(16x8, bf16, col).
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

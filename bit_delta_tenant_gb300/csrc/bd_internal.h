@@ -133,7 +133,16 @@ cudaError_t launch_decode_tma_multi(const BatchItem *items, int n, const DevCtx 
 cudaError_t launch_decode_batch(const BatchItem *items, int n, const BatchPlan &plan, void *workspace,
                                 const DevCtx &ctx, cudaStream_t stream);
 
-// Tensor-core (tcgen05 + TMA) kernel for any m.
+// Tensor-core kernel on CTA pairs (prefill_pair.cu): 256 W rows x 256 tokens per pair
+// of CTAs (tcgen05 cta_group::2), no K split.
+bool prefill_pair_supported(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx);
+int64_t prefill_pair_tiles(int64_t m, int64_t n_out);
+cudaError_t launch_prefill_pair(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                                int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                                cudaStream_t stream);
+
+// Tensor-core (tcgen05 + TMA) kernel for any m: CTA pairs when their tiles fill the
+// GPU, else one CTA per 128 x 256 tile (K split over a cluster when tiles are few).
 cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                            int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                            cudaStream_t stream);

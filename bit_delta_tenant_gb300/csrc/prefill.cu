@@ -530,6 +530,14 @@ cudaError_t launch_prefill_bn(const void *x, int64_t m, const void *w_base, cons
 cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                            int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                            cudaStream_t stream) {
+    // CTA pairs (256 x 256 tiles, half the activation traffic per SM) once their
+    // CTAs fill the SMs at least once; below that the single-CTA tiles, which can
+    // split K over a cluster to fill them.
+    const int64_t forced = option_value(BD_OPT_PREFILL_KERNEL);
+    const bool pair = forced == 2 || (forced == 0 && m > 64 &&
+                                      2 * prefill_pair_tiles(m, n_out) >= static_cast<int64_t>(ctx.num_sms));
+    if (pair && prefill_pair_supported(m, n_out, n_in, ctx))
+        return launch_prefill_pair(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
     if (m <= 64)
         return launch_prefill_bn<64>(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
     return launch_prefill_bn<256>(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);

@@ -1,0 +1,371 @@
+// prefill_pair.cu -- fused BitDelta linear for large token counts on CTA pairs:
+// y = x . (W_base + alpha*S)^T with W_eff rebuilt tile by tile on chip and
+// never written to HBM, one 256 (W rows) x 256 (tokens) output tile per pair
+// of CTAs on the 5th-generation tensor cores (tcgen05, cta_group::2).
+//
+// Method: "BitDelta : servir 14 modèles Zen depuis un seul cluster GPU"
+// (Hanzo blog), section "Architecture de service": the effective weight is
+// rebuilt on the fly by a fused kernel that reads the base weights and the
+// delta bits together, in registers or shared memory, and the reconstruction
+// is fused with the matrix multiply (conceptual fused_bitdelta_linear listing:
+// unpack to {-1,+1}, W_eff = W_base + alpha*unpacked, linear).
+//
+// Why pairs: with one CTA per 128 x 256 tile, every 64-wide K step moves the
+// whole 256-token activation tile into each SM's shared memory and the MMA
+// reads all of it again; a pair's MMA (M = 256 over both CTAs' tensor memory)
+// takes each CTA's half of the tokens from its own shared memory, so per SM
+// the activation fill and the operand reads are halved for the same FLOPs.
+//
+// A cluster of two CTAs (rank r = 0, 1) computes W rows [256*i + 128*r, +128)
+// of its tile in CTA r; per 64-wide K block:
+//   warp 0      TMA producer of this CTA: the W_base tile [128 x 64] of its
+//               own rows and its half of the token tile [N/2 x 64] (tokens
+//               n0 + r*N/2 ...), both K-major with the 128-byte swizzle, into a
+//               6-stage ring, completing on this CTA's full barrier.  No load
+//               is multicast: each CTA reads its own halves.
+//   warps 2..9  rebuild, in two groups of four taking alternate K blocks: one
+//               thread per W row, W_eff = W_base + alpha_b*s as bf16 pairs (one
+//               bf16x2 add per pair, alpha rounded to bf16), stored with
+//               tcgen05.st into this CTA's tensor memory as the MMA's A operand;
+//               then each warp arrives on the even CTA's "rebuilt" barrier.
+//               After the K loop the same warps are the epilogue (TMEM lanes
+//               32*(w%4)..+31, the groups splitting the token columns), writing
+//               y in bf16.
+//   warp 1      of the even CTA: one lane waits for both CTAs' rebuilt blocks
+//               and issues tcgen05.mma.cta_group::2 kind::f16 (M = 256,
+//               N = tokens <= 256, K = 16), committing each
+//               stage to the empty barriers of both CTAs (multicast commit).
+//               In both CTAs warp 1 allocates (and frees) the pair's tensor
+//               memory: 256 accumulator columns plus 32 per ring stage of A.
+// Every wait is bounded; a role that gives up records a timeout, its CTA
+// drains its own copies (and, in the even CTA, its MMAs), and both CTAs meet
+// at the closing cluster barrier before freeing tensor memory.
+#include "bd_device.cuh"
+#include "bd_internal.h"
+
+namespace bd {
+namespace {
+
+constexpr int kPM = 128;                  // W rows per CTA (half of the pair MMA's M)
+constexpr int kPN = 256;                  // tokens per pair tile (MMA N, at most)
+constexpr int kPK = 64;                   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kPStages = 6;
+constexpr uint32_t kPWBytes = kPM * kPK * 2;         // 16 KB
+constexpr uint32_t kPXBytes = (kPN / 2) * kPK * 2;   // 16 KB: this CTA's half of the tokens
+constexpr uint32_t kPStageTx = kPWBytes + kPXBytes;
+constexpr uint32_t kPAccCols = kPN;                  // fp32 accumulator columns (one per token)
+constexpr uint32_t kPTmemCols = 512;
+constexpr int kPRebuildWarps = 8;
+constexpr int kPThreads = (2 + kPRebuildWarps) * 32;
+constexpr size_t kPSmem = 1024 + kPStages * (kPWBytes + kPXBytes) + 256;
+static_assert(kPAccCols + kPStages * (kPK / 2) <= kPTmemCols, "accumulator + A stages fit in TMEM");
+
+struct PairArgs {
+    const uint8_t *bits;
+    const float *alpha;
+    uint16_t *y;
+    int64_t m, n_out, n_in;
+    int32_t mode;
+    int32_t num_kb;
+    int32_t row_tiles, tok_tiles, group;  // pair tiles: 256 W rows x 256 tokens
+    int32_t bits_vec8;                    // rows of packed bits are 8-byte aligned
+    unsigned *status;
+    uint64_t wait_ns;
+};
+
+template <int I>
+__device__ __forceinline__ uint32_t rebuild_pair_b(uint32_t w, uint32_t byte, uint32_t neg_alpha2) {
+    constexpr uint32_t mul = (1u << (15 - 2 * I)) + (1u << (30 - 2 * I));
+    const uint32_t s = ((byte * mul) & 0x80008000u) ^ neg_alpha2;
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(w), "r"(s));
+    return r;
+}
+
+__device__ __forceinline__ void give_up_p(volatile int *abort_flag, unsigned *status) {
+    *abort_flag = 1;
+    flag_status(status, kDevTimeout);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                        const __grid_constant__ PairArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sW = smem;
+    uint8_t *sX = smem + kPStages * kPWBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sX + kPStages * kPXBytes);
+    uint64_t *full = bars;                    // this CTA's TMA fills
+    uint64_t *rebuilt = bars + kPStages;      // even CTA: both CTAs' rebuilt A blocks
+    uint64_t *empty = bars + 2 * kPStages;    // the pair's MMAs of a stage are complete
+    uint64_t *acc_full = bars + 3 * kPStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const uint32_t rank = cluster_rank();
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    // Grouped rasterisation: consecutive pairs cycle over `group` token tiles for
+    // one W tile, so a wave touches a compact block of W and x in L2.
+    const int per_group = a.group * a.row_tiles;
+    const int grp = pair / per_group;
+    const int rem = pair - grp * per_group;
+    const int gsize = min(a.group, a.tok_tiles - grp * a.group);
+    const int tok_tile = grp * a.group + rem % gsize;
+    const int row_tile = rem / gsize;
+    const int m0 = row_tile * 2 * kPM + static_cast<int>(rank) * kPM;  // this CTA's W rows
+    const int n0 = tok_tile * kPN;                                     // the pair's first token
+    const int count = static_cast<int>(min(static_cast<int64_t>(kPN), a.m - n0));
+    const int n_mma = (count + 15) & ~15;  // pair MMA N; each CTA holds n_mma / 2 token rows
+    const int x_first = n0 + static_cast<int>(rank) * (n_mma / 2);
+    const int nkb = a.num_kb;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&rebuilt[s], kPRebuildWarps);  // four warps of the block's group in each CTA
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_x);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kPTmemCols);
+        tmem_relinquish_pair();
+    }
+    // Barriers initialised and tensor memory allocated in both CTAs before any
+    // remote arrive or multicast commit.
+    tc_fence_before();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kPStages;
+                const uint32_t ph = (kb / kPStages) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1, a.wait_ns, abort_flag)) {
+                    give_up_p(abort_flag, a.status);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], kPStageTx);
+                tma_load_2d(sW + s * kPWBytes, &tm_w, &full[s], kb * kPK, m0);
+                tma_load_2d(sX + s * kPXBytes, &tm_x, &full[s], kb * kPK, x_first);
+                issued = kb + 1;
+            }
+            if (*abort_flag) {
+                // the loads of the last stages issued land before the CTA may exit
+                for (int kb = (issued > kPStages ? issued - kPStages : 0); kb < issued; ++kb)
+                    mbar_wait(&full[kb % kPStages], (kb / kPStages) & 1, kDrainLimitNs, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc = idesc_bf16_f32(2 * kPM, n_mma);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int s = kb % kPStages;
+                const uint32_t ph = (kb / kPStages) & 1;
+                if (!mbar_wait(&rebuilt[s], ph, a.wait_ns, abort_flag)) {
+                    give_up_p(abort_flag, a.status);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t b_addr = smem_u32(sX + s * kPXBytes);
+#pragma unroll
+                for (int kk = 0; kk < kPK / 16; ++kk)
+                    tc_mma_f16_ts_pair(tmem, tmem + kPAccCols + s * (kPK / 2) + kk * 8,
+                                       sw128_kmajor_desc(b_addr + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+                tc_commit_pair_mc(&empty[s], 0x3);
+            }
+            // Always: both CTAs' epilogues wait for this, and this thread's MMAs are
+            // complete before the pair may free tensor memory.
+            tc_commit_pair_mc(acc_full, 0x3);
+            mbar_wait(acc_full, 0, kDrainLimitNs, nullptr);
+        }
+    } else {
+        // ---- rebuild (then epilogue) warps ------------------------------------------
+        // Thread q of group h (warps 2..5: h = 0, warps 6..9: h = 1) owns tile row
+        // r = 32*(warp%4) + lane: all eight 16-byte chunks of the row (its 8 packed
+        // bytes) in the K blocks of parity h.  Warp w may access TMEM lanes
+        // 32*(w%4)..+31 only, so the same row mapping serves the epilogue, where h
+        // picks half of the token columns.
+        const int sub = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const int r = sub * 32 + lane;
+        const int64_t row = static_cast<int64_t>(m0) + r;
+        const bool row_ok = row < a.n_out;
+        const float al = row_ok ? (a.mode ? a.alpha[row] : a.alpha[0]) : 0.0f;
+        const uint32_t neg_al = pack_bf16x2(-al, -al);  // -alpha_b in both halves
+        const int64_t bpr = a.n_in / 8;
+        const uint8_t *brow = a.bits + (row_ok ? row : 0) * bpr;
+        const uint32_t rebuilt0 = mapa_rank(smem_u32(rebuilt), 0);  // the even CTA's barriers
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>(sub * 32) << 16) + kPAccCols;
+
+        auto load_bits = [&](int kb) -> uint2 {
+            uint2 v = make_uint2(0u, 0u);
+            const int64_t c0 = static_cast<int64_t>(kb) * 8;  // first packed byte of the block
+            if (row_ok && kb < nkb) {
+                if (a.bits_vec8 && c0 + 8 <= bpr) {
+                    v = __ldg(reinterpret_cast<const uint2 *>(brow + c0));
+                } else {
+                    for (int c = 0; c < 8; ++c)
+                        if (c0 + c < bpr) {
+                            const uint32_t byte = __ldg(brow + c0 + c);
+                            if (c < 4) v.x |= byte << (8 * c);
+                            else v.y |= byte << (8 * (c - 4));
+                        }
+                }
+            }
+            return v;
+        };
+
+        // Packed bits arrive by plain loads three of this group's K blocks ahead.
+        constexpr int kBitsAhead = 3;
+        uint2 bq[kBitsAhead];
+#pragma unroll
+        for (int i = 0; i < kBitsAhead; ++i) bq[i] = load_bits(h + 2 * i);
+        bool ok = true;
+        for (int kb = h; kb < nkb; kb += 2) {
+            const int s = kb % kPStages;
+            const uint32_t ph = (kb / kPStages) & 1;
+            const uint2 b_cur = bq[0];
+#pragma unroll
+            for (int i = 0; i + 1 < kBitsAhead; ++i) bq[i] = bq[i + 1];
+            bq[kBitsAhead - 1] = load_bits(kb + 2 * kBitsAhead);
+            const bool got = mbar_wait(&full[s], ph, a.wait_ns, abort_flag);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                if (lane == 0) give_up_p(abort_flag, a.status);
+                ok = false;
+                break;
+            }
+            const uint8_t *rowp = sW + s * kPWBytes + r * 128;
+            uint32_t v[32];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(rowp + ((cc ^ (r & 7)) << 4));
+                const uint32_t byte = ((cc < 4 ? b_cur.x : b_cur.y) >> (8 * (cc & 3))) & 0xFFu;
+                v[4 * cc + 0] = rebuild_pair_b<0>(w.x, byte, neg_al);
+                v[4 * cc + 1] = rebuild_pair_b<1>(w.y, byte, neg_al);
+                v[4 * cc + 2] = rebuild_pair_b<2>(w.z, byte, neg_al);
+                v[4 * cc + 3] = rebuild_pair_b<3>(w.w, byte, neg_al);
+            }
+            tmem_st_32x32b_x32(a_lane + s * (kPK / 2), v);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(rebuilt0 + static_cast<uint32_t>(s) * 8u);
+        }
+        if (ok) {
+            const bool got = mbar_wait(acc_full, 0, a.wait_ns, abort_flag);
+            if (__all_sync(0xFFFFFFFFu, got)) {
+                tc_fence_after();
+                const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+                uint16_t *ycol = a.y + row;
+#pragma unroll 1
+                for (int c0 = h * (kPN / 2); c0 < (h + 1) * (kPN / 2); c0 += 32) {
+                    if (c0 >= count) break;  // warp-uniform
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(lane_addr + c0, v);
+                    tmem_ld_wait();
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            if (c0 + i < count) {
+                                __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[i]));
+                                ycol[(static_cast<int64_t>(n0) + c0 + i) * a.n_out] = *reinterpret_cast<uint16_t *>(&hv);
+                            }
+                        }
+                    }
+                }
+            } else if (lane == 0) {
+                give_up_p(abort_flag, a.status);
+            }
+        }
+    }
+
+    // Both CTAs are done with the pair's tensor memory (the even CTA's MMAs have
+    // completed and every epilogue has read its accumulator) before it is freed.
+    tc_fence_before();
+    __syncthreads();
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, kPTmemCols);
+}
+
+}  // namespace
+
+bool prefill_pair_supported(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx) {
+    if (m < 1 || n_out < 1 || n_in < 8 || ctx.num_sms < 2) return false;
+    const int64_t pairs = ((n_out + 2 * kPM - 1) / (2 * kPM)) * ((m + kPN - 1) / kPN);
+    return 2 * pairs <= 0x7FFFFFFFLL;
+}
+
+// Pair tiles of the shape: 256 W rows x 256 tokens.
+int64_t prefill_pair_tiles(int64_t m, int64_t n_out) {
+    return ((n_out + 2 * kPM - 1) / (2 * kPM)) * ((m + kPN - 1) / kPN);
+}
+
+cudaError_t launch_prefill_pair(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                                int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                                cudaStream_t stream) {
+    if (!prefill_pair_supported(m, n_out, n_in, ctx)) return cudaErrorNotSupported;
+    static bool attr_set[128] = {false};
+    if (ctx.device < 128 && !attr_set[ctx.device]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kPSmem));
+        if (e != cudaSuccess) return e;
+        attr_set[ctx.device] = true;
+    }
+    CUtensorMap tm_w, tm_x;
+    if (!encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kPK, kPM,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, m, n_in * 2, kPK, kPN / 2,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    PairArgs a = {};
+    a.bits = bits;
+    a.alpha = alpha;
+    a.y = static_cast<uint16_t *>(y);
+    a.m = m;
+    a.n_out = n_out;
+    a.n_in = n_in;
+    a.mode = alpha_mode;
+    a.num_kb = static_cast<int32_t>((n_in + kPK - 1) / kPK);
+    a.row_tiles = static_cast<int32_t>((n_out + 2 * kPM - 1) / (2 * kPM));
+    a.tok_tiles = static_cast<int32_t>((m + kPN - 1) / kPN);
+    a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
+    a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
+    const int64_t grid = 2 * static_cast<int64_t>(a.row_tiles) * a.tok_tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kPThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tm_w, tm_x, a);
+}
+
+}  // namespace bd

@@ -441,6 +441,9 @@ int32_t bd_set_weight_prefetch(int32_t enable);
  *                         bd_linear
  *   BD_OPT_BATCH_GRID     CTAs of an evenly split batched launch (1 ..
  *                         2^31-1, capped at the CTAs that fit at once)
+ *   BD_OPT_PREFILL_KERNEL tensor-core linear (m > 64): 0 automatic; 1 one
+ *                         CTA per 128 x 256 tile (K split over a cluster when
+ *                         tiles are few); 2 CTA pairs on 256 x 256 tiles
  *   BD_OPT_TEST_STALL     1 makes the first pipeline wait of the kernels
  *                         that support it -- the persistent compression
  *                         form and the multi-tenant streaming kernels --
@@ -456,6 +459,7 @@ int32_t bd_set_weight_prefetch(int32_t enable);
 #define BD_OPT_BATCH_SINGLE 4
 #define BD_OPT_BATCH_GRID 5
 #define BD_OPT_TEST_STALL 6
+#define BD_OPT_PREFILL_KERNEL 7
 int64_t bd_set_option(int32_t option, int64_t value);
 
 /* Library version, major * 10000 + minor * 100 + patch. */

@@ -63,21 +63,39 @@ def test_streaming_kernel_shapes(n_out, n_in, m, mode, path):
     full_check(case, path, f"stream path={path} {n_out}x{n_in} m={m}")
 
 
-TENSOR_SHAPES = [  # ragged in every dimension: rows vs 128, tokens vs 256, K vs 64
+TENSOR_SHAPES = [  # ragged in every dimension: rows vs 128/256, tokens vs 256, K vs 64
     (128, 64, 256), (129, 64, 1), (7, 8, 5), (128, 72, 257), (300, 136, 100), (256, 1024, 511),
-    (200, 520, 512), (384, 4096, 513), (129, 24, 65), (64, 4104, 300),
+    (200, 520, 512), (384, 4096, 513), (129, 24, 65), (64, 4104, 300), (257, 640, 9), (513, 192, 16),
+    (1000, 2048, 263), (520, 4096, 1024),
 ]
+# the tensor-core kernels: one CTA per 128 x 256 tile, and CTA pairs on 256 x 256 tiles
+PREFILL_KERNELS = {"single": 1, "pair": 2}
+
+
+@pytest.fixture(params=list(PREFILL_KERNELS))
+def prefill_kernel(request):
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, PREFILL_KERNELS[request.param]):
+        yield request.param
 
 
 @pytest.mark.parametrize("n_out,n_in,m", TENSOR_SHAPES)
 @pytest.mark.parametrize("mode", [0, 1])
-def test_tensor_core_kernel_shapes(n_out, n_in, m, mode):
+def test_tensor_core_kernel_shapes(n_out, n_in, m, mode, prefill_kernel):
     case = LinearCase(n_out, n_in, m, 0.02, "row:5e-4:2e-3" if mode else 1e-3, mode, seed=3 * n_out + n_in + m)
-    full_check(case, TENSOR, f"tcgen05 {n_out}x{n_in} m={m}")
+    full_check(case, TENSOR, f"tcgen05 {prefill_kernel} {n_out}x{n_in} m={m}")
+
+
+@pytest.mark.parametrize("m", [1, 8, 9, 16, 17, 120, 128, 129, 255, 256])
+def test_pair_kernel_last_token_tile_split(m):
+    """The pair's MMA N is the tile's token count rounded to 16, each CTA holding half of it:
+    a last tile of few tokens leaves the odd CTA's half partly or wholly past the end."""
+    case = LinearCase(300, 512, 256 + m, seed=40 + m)
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, 2):
+        full_check(case, TENSOR, f"pair m={256 + m}")
 
 
 @pytest.mark.parametrize("path", [STREAM, STREAM_REG, TENSOR])
-def test_alpha_zero_is_plain_base_linear(path):
+def test_alpha_zero_is_plain_base_linear(path, prefill_kernel):
     case = LinearCase(96, 256, 16, seed=11)
     case.alpha.zero_()
     case.alpha32_h[:] = 0
@@ -86,7 +104,7 @@ def test_alpha_zero_is_plain_base_linear(path):
 
 @pytest.mark.parametrize("path", [STREAM, STREAM_REG, TENSOR])
 @pytest.mark.parametrize("n_in", [32, 128])
-def test_zero_base_unit_alpha_is_exact_sign_product(path, n_in):
+def test_zero_base_unit_alpha_is_exact_sign_product(path, n_in, prefill_kernel):
     """W_base = 0, alpha = 1, integer x: y = x . S^T exactly (|y| <= 2*n_in fits bf16 exactly here)."""
     rng = np.random.default_rng(3)
     n_out, m = 64, 8
@@ -174,7 +192,7 @@ def test_repeated_calls_on_a_side_stream():
     assert_y_close(y_host(y1), y_ref, mag, "side stream")
 
 
-def test_wait_limit_zero_reports_timeout_and_context_survives():
+def test_wait_limit_zero_reports_timeout_and_context_survives(prefill_kernel):
     """A zero wait limit makes the tensor-core kernel give up at its first
     unsatisfied wait: it records a timeout, drains its own copies and returns.
     The context stays usable and a normal call afterwards is correct."""
