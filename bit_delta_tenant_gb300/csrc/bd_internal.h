@@ -168,6 +168,10 @@ struct GroupTable {
 cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
                                    int64_t n_out, int64_t n_in, void *y, const GroupTable &tab, const DevCtx &ctx,
                                    cudaStream_t stream);
+// The same on CTA pairs: 256 W rows per pair and a token tile of one variant.
+cudaError_t launch_prefill_pair_grouped(const void *x_sorted, int64_t m, const void *w_base,
+                                        const GroupedVariants &vars, int64_t n_out, int64_t n_in, void *y,
+                                        const GroupTable &tab, const DevCtx &ctx, cudaStream_t stream);
 
 // Tensor-core streaming multi-tenant kernel for small batches (grouped_decode_tc.cu).
 bool grouped_decode_tc_supported(int64_t m, int32_t n_variants, int64_t n_in, const void *x_sorted,

@@ -553,6 +553,13 @@ cudaError_t launch_base_product(const void *x, int64_t m, const void *w_base, in
 cudaError_t launch_prefill_grouped(const void *x_sorted, int64_t m, const void *w_base, const GroupedVariants &vars,
                                    int64_t n_out, int64_t n_in, void *y, const GroupTable &tab, const DevCtx &ctx,
                                    cudaStream_t stream) {
+    // CTA pairs when the tiles of the dense token count would fill the SMs (as for one variant)
+    const int64_t forced = option_value(BD_OPT_PREFILL_KERNEL);
+    const bool pair = forced == 2 || (forced == 0 && 2 * prefill_pair_tiles(m, n_out) >= static_cast<int64_t>(ctx.num_sms));
+    if (pair) {
+        const cudaError_t e = launch_prefill_pair_grouped(x_sorted, m, w_base, vars, n_out, n_in, y, tab, ctx, stream);
+        if (e != cudaErrorNotSupported) return e;
+    }
     const bool tmem_a = use_tmem_a();
     cudaError_t e = tmem_a ? set_smem_attr<true, true, 256>(ctx) : set_smem_attr<true, false, 256>(ctx);
     if (e != cudaSuccess) return e;

@@ -60,6 +60,8 @@ constexpr int kPThreads = (2 + kPRebuildWarps) * 32;
 constexpr size_t kPSmem = 1024 + kPStages * (kPWBytes + kPXBytes) + 256;
 static_assert(kPAccCols + kPStages * (kPK / 2) <= kPTmemCols, "accumulator + A stages fit in TMEM");
 
+constexpr int kPMaxVariants = 64;
+
 struct PairArgs {
     const uint8_t *bits;
     const float *alpha;
@@ -71,6 +73,17 @@ struct PairArgs {
     int32_t bits_vec8;                    // rows of packed bits are 8-byte aligned
     unsigned *status;
     uint64_t wait_ns;
+    // Multi-tenant mode only: token tiles come from a device-built table of
+    // (variant, first row in the variant-sorted activations, row count <= 256);
+    // consecutive pairs take every slot of one 256-row W tile, and output rows
+    // are scattered back to the original token order through perm.
+    const int32_t *tiles;
+    const int32_t *n_tiles;
+    const int32_t *perm;
+    int32_t max_slots;
+    const uint8_t *vbits[kPMaxVariants];
+    const float *valpha[kPMaxVariants];
+    int32_t vmode[kPMaxVariants];
 };
 
 template <int I>
@@ -93,6 +106,7 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                         const __grid_constant__ PairArgs a) {
@@ -110,17 +124,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     const uint32_t rank = cluster_rank();
     const int pair = static_cast<int>(blockIdx.x >> 1);
-    // Grouped rasterisation: consecutive pairs cycle over `group` token tiles for
-    // one W tile, so a wave touches a compact block of W and x in L2.
-    const int per_group = a.group * a.row_tiles;
-    const int grp = pair / per_group;
-    const int rem = pair - grp * per_group;
-    const int gsize = min(a.group, a.tok_tiles - grp * a.group);
-    const int tok_tile = grp * a.group + rem % gsize;
-    const int row_tile = rem / gsize;
+    int row_tile, n0, count;
+    const uint8_t *bits;
+    const float *alpha;
+    int32_t mode;
+    if constexpr (kGrouped) {
+        // Consecutive pairs take every token tile of one W tile, so the W tile is
+        // read from HBM once per wave and reused from L2.
+        row_tile = pair / a.max_slots;
+        const int slot = pair - row_tile * a.max_slots;
+        if (slot >= *a.n_tiles) return;  // the same for both CTAs, before any barrier or TMEM use
+        const int v = a.tiles[3 * slot];
+        n0 = a.tiles[3 * slot + 1];
+        count = a.tiles[3 * slot + 2];
+        bits = a.vbits[v];
+        alpha = a.valpha[v];
+        mode = a.vmode[v];
+    } else {
+        // Grouped rasterisation: consecutive pairs cycle over `group` token tiles for
+        // one W tile, so a wave touches a compact block of W and x in L2.
+        const int per_group = a.group * a.row_tiles;
+        const int grp = pair / per_group;
+        const int rem = pair - grp * per_group;
+        const int gsize = min(a.group, a.tok_tiles - grp * a.group);
+        const int tok_tile = grp * a.group + rem % gsize;
+        row_tile = rem / gsize;
+        n0 = tok_tile * kPN;  // the pair's first token
+        count = static_cast<int>(min(static_cast<int64_t>(kPN), a.m - n0));
+        bits = a.bits;
+        alpha = a.alpha;
+        mode = a.mode;
+    }
     const int m0 = row_tile * 2 * kPM + static_cast<int>(rank) * kPM;  // this CTA's W rows
-    const int n0 = tok_tile * kPN;                                     // the pair's first token
-    const int count = static_cast<int>(min(static_cast<int64_t>(kPN), a.m - n0));
     const int n_mma = (count + 15) & ~15;  // pair MMA N; each CTA holds n_mma / 2 token rows
     const int x_first = n0 + static_cast<int>(rank) * (n_mma / 2);
     const int nkb = a.num_kb;
@@ -208,10 +243,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int r = sub * 32 + lane;
         const int64_t row = static_cast<int64_t>(m0) + r;
         const bool row_ok = row < a.n_out;
-        const float al = row_ok ? (a.mode ? a.alpha[row] : a.alpha[0]) : 0.0f;
+        const float al = row_ok ? (mode ? alpha[row] : alpha[0]) : 0.0f;
         const uint32_t neg_al = pack_bf16x2(-al, -al);  // -alpha_b in both halves
         const int64_t bpr = a.n_in / 8;
-        const uint8_t *brow = a.bits + (row_ok ? row : 0) * bpr;
+        const uint8_t *brow = bits + (row_ok ? row : 0) * bpr;
         const uint32_t rebuilt0 = mapa_rank(smem_u32(rebuilt), 0);  // the even CTA's barriers
         const uint32_t a_lane = tmem + (static_cast<uint32_t>(sub * 32) << 16) + kPAccCols;
 
@@ -285,8 +320,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             if (c0 + i < count) {
+                                const int64_t t = kGrouped ? static_cast<int64_t>(a.perm[n0 + c0 + i])
+                                                           : static_cast<int64_t>(n0) + c0 + i;
                                 __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[i]));
-                                ycol[(static_cast<int64_t>(n0) + c0 + i) * a.n_out] = *reinterpret_cast<uint16_t *>(&hv);
+                                ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&hv);
                             }
                         }
                     }
@@ -320,41 +357,27 @@ int64_t prefill_pair_tiles(int64_t m, int64_t n_out) {
     return ((n_out + 2 * kPM - 1) / (2 * kPM)) * ((m + kPN - 1) / kPN);
 }
 
-cudaError_t launch_prefill_pair(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
-                                int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
-                                cudaStream_t stream) {
-    if (!prefill_pair_supported(m, n_out, n_in, ctx)) return cudaErrorNotSupported;
+namespace {
+
+template <bool kGrouped>
+cudaError_t launch_pair(const PairArgs &a, const void *w_base, const void *x, int64_t x_rows, int64_t pairs,
+                        const DevCtx &ctx, cudaStream_t stream) {
     static bool attr_set[128] = {false};
     if (ctx.device < 128 && !attr_set[ctx.device]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kPSmem));
+        cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<kGrouped>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kPSmem));
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
     CUtensorMap tm_w, tm_x;
-    if (!encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kPK, kPM,
+    if (!encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, a.n_in, a.n_out, a.n_in * 2, kPK, kPM,
                               CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, m, n_in * 2, kPK, kPN / 2,
+        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.n_in, x_rows, a.n_in * 2, kPK, kPN / 2,
                               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    PairArgs a = {};
-    a.bits = bits;
-    a.alpha = alpha;
-    a.y = static_cast<uint16_t *>(y);
-    a.m = m;
-    a.n_out = n_out;
-    a.n_in = n_in;
-    a.mode = alpha_mode;
-    a.num_kb = static_cast<int32_t>((n_in + kPK - 1) / kPK);
-    a.row_tiles = static_cast<int32_t>((n_out + 2 * kPM - 1) / (2 * kPM));
-    a.tok_tiles = static_cast<int32_t>((m + kPN - 1) / kPN);
-    a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
-    a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
-    a.status = ctx.status;
-    a.wait_ns = ctx.wait_ns;
-    const int64_t grid = 2 * static_cast<int64_t>(a.row_tiles) * a.tok_tiles;
+    if (2 * pairs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     cfg.blockDim = dim3(kPThreads, 1, 1);
     cfg.dynamicSmemBytes = kPSmem;
     cfg.stream = stream;
@@ -365,7 +388,56 @@ cudaError_t launch_prefill_pair(const void *x, int64_t m, const void *w_base, co
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel, tm_w, tm_x, a);
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<kGrouped>, tm_w, tm_x, a);
+}
+
+void fill_pair_common(PairArgs &a, int64_t m, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx) {
+    a.y = static_cast<uint16_t *>(y);
+    a.m = m;
+    a.n_out = n_out;
+    a.n_in = n_in;
+    a.num_kb = static_cast<int32_t>((n_in + kPK - 1) / kPK);
+    a.row_tiles = static_cast<int32_t>((n_out + 2 * kPM - 1) / (2 * kPM));
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_pair(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
+                                int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
+                                cudaStream_t stream) {
+    if (!prefill_pair_supported(m, n_out, n_in, ctx)) return cudaErrorNotSupported;
+    PairArgs a = {};
+    fill_pair_common(a, m, n_out, n_in, y, ctx);
+    a.bits = bits;
+    a.alpha = alpha;
+    a.mode = alpha_mode;
+    a.tok_tiles = static_cast<int32_t>((m + kPN - 1) / kPN);
+    a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
+    a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
+    return launch_pair<false>(a, w_base, x, m, static_cast<int64_t>(a.row_tiles) * a.tok_tiles, ctx, stream);
+}
+
+cudaError_t launch_prefill_pair_grouped(const void *x_sorted, int64_t m, const void *w_base,
+                                        const GroupedVariants &vars, int64_t n_out, int64_t n_in, void *y,
+                                        const GroupTable &tab, const DevCtx &ctx, cudaStream_t stream) {
+    if (!prefill_pair_supported(m, n_out, n_in, ctx) || vars.count > kPMaxVariants) return cudaErrorNotSupported;
+    PairArgs a = {};
+    fill_pair_common(a, m, n_out, n_in, y, ctx);
+    bool vec8 = (n_in / 8) % 8 == 0;
+    for (int v = 0; v < vars.count; ++v) {
+        a.vbits[v] = vars.bits[v];
+        a.valpha[v] = vars.alpha[v];
+        a.vmode[v] = vars.mode[v];
+        vec8 = vec8 && (reinterpret_cast<uintptr_t>(vars.bits[v]) & 7) == 0;
+    }
+    a.bits_vec8 = vec8 ? 1 : 0;
+    a.tiles = tab.tiles;
+    a.n_tiles = tab.n_tiles;
+    a.perm = tab.perm;
+    a.max_slots = tab.max_slots;
+    return launch_pair<true>(a, w_base, x_sorted, m, static_cast<int64_t>(a.row_tiles) * tab.max_slots, ctx, stream);
 }
 
 }  // namespace bd

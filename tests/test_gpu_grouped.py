@@ -81,12 +81,30 @@ def test_uniform_ids_fourteen_variants(m):
     check_full(case, f"14 variants m={m}")
 
 
-def test_zipf_segments_fourteen_variants():
+@pytest.fixture(params=["single", "pair"])
+def prefill_kernel(request):
+    """The tensor-core kernel of the per-variant token tiles: one CTA per 128 W rows, or CTA pairs
+    on 256 W rows (BD_OPT_PREFILL_KERNEL)."""
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, 1 if request.param == "single" else 2):
+        yield request.param
+
+
+def test_zipf_segments_fourteen_variants(prefill_kernel):
     ids = synth.zipf_ids(2048, 14, 1.1, seed=5)
     assert sorted(np.bincount(ids, minlength=14).tolist(), reverse=True) == \
         [699, 326, 209, 152, 119, 97, 82, 71, 62, 56, 50, 45, 42, 38]
     case = GroupedCase(200, 520, 14, ids, seed=6)
-    check_full(case, "zipf")
+    check_full(case, f"zipf {prefill_kernel}")
+
+
+@pytest.mark.parametrize("n_out,n_in,m,n_var", [(257, 640, 300, 5), (513, 192, 1000, 14), (100, 4096, 65, 3),
+                                                 (384, 1024, 777, 64)])
+def test_tensor_core_tiles_ragged_shapes(n_out, n_in, m, n_var, prefill_kernel):
+    """Per-variant token tiles on both tensor-core kernels: ragged W rows (vs 128 and 256), ragged
+    K, tiles of a few tokens, up to 64 variants with mixed alpha modes."""
+    ids = synth.uniform_ids(m, n_var, seed=n_out + m)
+    case = GroupedCase(n_out, n_in, n_var, ids, modes=[v % 2 for v in range(n_var)], seed=n_in + m)
+    check_full(case, f"{prefill_kernel} {n_out}x{n_in} m={m} V={n_var}")
 
 
 def test_empty_variants_and_all_tokens_in_one_variant():
