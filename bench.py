@@ -331,7 +331,11 @@ class LayerWorkload(Workload):
                     if need > 0 and (self.batch_ws is None or self.batch_ws.numel() < need):
                         self.batch_ws = torch.zeros(need, dtype=torch.uint8, device=dev)
                     calls.append(lambda descs=descs: bd.bd_linear_batch(descs, self.batch_ws))
-                    batched = m <= 16 and all(p[1].shape[1] % 128 == 0 for p in probs)
+                    # one launch: the batched streaming kernel (m <= 16), or the pair kernel over the
+                    # group (m > 64) when its 256 x 256 tiles fill the SMs (152 on GB300)
+                    pair_tiles = sum(-(-p[5].shape[1] // 256) * -(-m // 256) for p in probs)
+                    batched = len(probs) > 1 and ((m <= 16 and all(p[1].shape[1] % 128 == 0 for p in probs))
+                                                  or (m > 64 and 2 * pair_tiles >= 152))
                     launches += 1 if batched else len(probs)
                 else:
                     x, wb, bits, alpha, _, y = probs[0]

@@ -321,7 +321,8 @@ int32_t run_linear(const void *x, int64_t m, const void *w_base, const uint8_t *
 // (problems grouped by m <= 8 / m <= 16, at most kBatchMaxProblems each) and
 // problems that run alone.
 struct BatchSchedule {
-    std::vector<std::vector<bd::BatchItem>> launches;
+    std::vector<std::vector<bd::BatchItem>> launches;       // batched streaming kernels (m <= 16)
+    std::vector<std::vector<bd::BatchItem>> pair_launches;  // tensor-core pair kernel over several linears
     std::vector<int32_t> alone;
 };
 int32_t schedule_batch(const bd_linear_desc *d, int32_t n, BatchSchedule &out) {
@@ -338,13 +339,36 @@ int32_t schedule_batch(const bd_linear_desc *d, int32_t n, BatchSchedule &out) {
     // (the cluster-split kernel) unless the BD_OPT_BATCH_SINGLE option keeps it (tests).
     const size_t min_size = bd::option_value(BD_OPT_BATCH_SINGLE) == 1 ? 1 : 2;
     std::vector<int32_t> group[2];  // problems of the batched kernel, by token tiles
+    std::vector<int32_t> tensor;    // problems for the pair kernel (m > 64)
+    const bool pairs_ok = bd::option_value(BD_OPT_PREFILL_KERNEL) != 1;
     for (int32_t i = 0; i < n; ++i) {
         const bd_linear_desc &q = d[i];
         if (q.m == 0) continue;
         if ((path == 0 || path == 1) && bd::decode_batch_supported(q.m, q.n_out, q.n_in, q.x, q.w_base, q.bits, q.y))
             group[q.m <= 8 ? 0 : 1].push_back(i);
+        else if ((path == 0 || path == 2) && pairs_ok && q.m > 64)
+            tensor.push_back(i);
         else
             out.alone.push_back(i);
+    }
+    // Pair-kernel launches of up to kPairMaxLinears problems when their pair tiles together fill
+    // the SMs (fewer tiles: each runs as bd_linear, which may split K on single-CTA tiles).
+    bd::DevCtx ctx;
+    const bool have_ctx = !tensor.empty() && make_ctx(&ctx) == BD_OK;
+    for (size_t first = 0; first < tensor.size(); first += bd::kPairMaxLinears) {
+        const size_t count = std::min(tensor.size() - first, static_cast<size_t>(bd::kPairMaxLinears));
+        std::vector<bd::BatchItem> items;
+        int64_t tiles = 0;
+        for (size_t k = first; k < first + count; ++k) {
+            const bd_linear_desc &q = d[tensor[k]];
+            items.push_back({q.x, q.w_base, q.bits, q.alpha, q.y, q.m, q.n_out, q.n_in, q.alpha_mode});
+            tiles += bd::prefill_pair_tiles(q.m, q.n_out);
+        }
+        if (count >= 2 && have_ctx && 2 * tiles >= ctx.num_sms &&
+            bd::prefill_pair_multi_supported(items.data(), static_cast<int>(count), ctx))
+            out.pair_launches.push_back(items);
+        else
+            out.alone.insert(out.alone.end(), tensor.begin() + first, tensor.begin() + first + count);
     }
     for (const auto &g : group) {
         for (size_t first = 0; first < g.size(); first += bd::kBatchMaxProblems) {
@@ -395,7 +419,7 @@ BD_API int32_t bd_linear_batch(const bd_linear_desc *descs, int32_t n, void *wor
     BatchSchedule sch;
     const int32_t v = schedule_batch(descs, n, sch);
     if (v != BD_OK) return v;
-    if (sch.launches.empty() && sch.alone.empty()) return BD_OK;
+    if (sch.launches.empty() && sch.pair_launches.empty() && sch.alone.empty()) return BD_OK;
     bd::DevCtx ctx;
     const int32_t rc = make_ctx(&ctx);
     if (rc != BD_OK) return rc;
@@ -421,6 +445,10 @@ BD_API int32_t bd_linear_batch(const bd_linear_desc *descs, int32_t n, void *wor
         const int32_t r = cluster && bd::decode_tma_multi_supported(items, cnt)
                               ? cuda_status(bd::launch_decode_tma_multi(items, cnt, ctx, s))
                               : cuda_status(bd::launch_decode_batch(items, cnt, plans[i], workspace, ctx, s));
+        if (r != BD_OK) return r;
+    }
+    for (const auto &g : sch.pair_launches) {
+        const int32_t r = cuda_status(bd::launch_prefill_pair_multi(g.data(), static_cast<int>(g.size()), ctx, s));
         if (r != BD_OK) return r;
     }
     for (int32_t i : sch.alone) {

@@ -137,6 +137,11 @@ cudaError_t launch_decode_batch(const BatchItem *items, int n, const BatchPlan &
 // of CTAs (tcgen05 cta_group::2), no K split.
 bool prefill_pair_supported(int64_t m, int64_t n_out, int64_t n_in, const DevCtx &ctx);
 int64_t prefill_pair_tiles(int64_t m, int64_t n_out);
+// Up to 8 independent linears (m > 64 each) in one launch of the pair kernel, their pair
+// tiles numbered linear by linear (a layer's q/k/v or gate/up share one wave sequence).
+constexpr int kPairMaxLinears = 8;
+bool prefill_pair_multi_supported(const BatchItem *items, int n, const DevCtx &ctx);
+cudaError_t launch_prefill_pair_multi(const BatchItem *items, int n, const DevCtx &ctx, cudaStream_t stream);
 cudaError_t launch_prefill_pair(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                                 int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                                 cudaStream_t stream);

@@ -61,8 +61,10 @@ constexpr size_t kPSmem = 1024 + kPStages * (kPWBytes + kPXBytes) + 256;
 static_assert(kPAccCols + kPStages * (kPK / 2) <= kPTmemCols, "accumulator + A stages fit in TMEM");
 
 constexpr int kPMaxVariants = 64;
+constexpr int kPMaxLinears = 8;  // independent linears per launch (a layer's q/k/v, gate/up)
 
-struct PairArgs {
+// One linear of a launch: its pairs are [first_pair, first_pair + row_tiles * tok_tiles).
+struct PairLinear {
     const uint8_t *bits;
     const float *alpha;
     uint16_t *y;
@@ -71,6 +73,17 @@ struct PairArgs {
     int32_t num_kb;
     int32_t row_tiles, tok_tiles, group;  // pair tiles: 256 W rows x 256 tokens
     int32_t bits_vec8;                    // rows of packed bits are 8-byte aligned
+    int32_t first_pair;
+};
+
+struct PairMaps {
+    CUtensorMap w[kPMaxLinears];  // W_base [n_out, n_in], boxes of 64 x 128 rows
+    CUtensorMap x[kPMaxLinears];  // x [m, n_in], boxes of 64 x 128 token rows
+};
+
+struct PairArgs {
+    PairLinear lin[kPMaxLinears];
+    int32_t n_lin;
     unsigned *status;
     uint64_t wait_ns;
     // Multi-tenant mode only: token tiles come from a device-built table of
@@ -108,8 +121,7 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 
 template <bool kGrouped>
 __global__ void __launch_bounds__(kPThreads, 1)
-    prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                        const __grid_constant__ PairArgs a) {
+    prefill_pair_kernel(const __grid_constant__ PairMaps maps, const __grid_constant__ PairArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;
@@ -123,7 +135,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const uint32_t rank = cluster_rank();
-    const int pair = static_cast<int>(blockIdx.x >> 1);
+    int lp = 0;  // this pair's linear
+    while (lp + 1 < a.n_lin && a.lin[lp + 1].first_pair <= static_cast<int>(blockIdx.x >> 1)) ++lp;
+    const PairLinear &L = a.lin[lp];
+    const CUtensorMap *tm_w = &maps.w[lp], *tm_x = &maps.x[lp];
+    const int pair = static_cast<int>(blockIdx.x >> 1) - L.first_pair;
     int row_tile, n0, count;
     const uint8_t *bits;
     const float *alpha;
@@ -143,22 +159,22 @@ __global__ void __launch_bounds__(kPThreads, 1)
     } else {
         // Grouped rasterisation: consecutive pairs cycle over `group` token tiles for
         // one W tile, so a wave touches a compact block of W and x in L2.
-        const int per_group = a.group * a.row_tiles;
+        const int per_group = L.group * L.row_tiles;
         const int grp = pair / per_group;
         const int rem = pair - grp * per_group;
-        const int gsize = min(a.group, a.tok_tiles - grp * a.group);
-        const int tok_tile = grp * a.group + rem % gsize;
+        const int gsize = min(L.group, L.tok_tiles - grp * L.group);
+        const int tok_tile = grp * L.group + rem % gsize;
         row_tile = rem / gsize;
         n0 = tok_tile * kPN;  // the pair's first token
-        count = static_cast<int>(min(static_cast<int64_t>(kPN), a.m - n0));
-        bits = a.bits;
-        alpha = a.alpha;
-        mode = a.mode;
+        count = static_cast<int>(min(static_cast<int64_t>(kPN), L.m - n0));
+        bits = L.bits;
+        alpha = L.alpha;
+        mode = L.mode;
     }
     const int m0 = row_tile * 2 * kPM + static_cast<int>(rank) * kPM;  // this CTA's W rows
     const int n_mma = (count + 15) & ~15;  // pair MMA N; each CTA holds n_mma / 2 token rows
     const int x_first = n0 + static_cast<int>(rank) * (n_mma / 2);
-    const int nkb = a.num_kb;
+    const int nkb = L.num_kb;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -172,8 +188,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_init(acc_full, 1);
         *abort_flag = 0;
         mbar_fence_init();
-        tma_prefetch_desc(&tm_w);
-        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(tm_w);
+        tma_prefetch_desc(tm_x);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, kPTmemCols);
@@ -198,8 +214,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&full[s], kPStageTx);
-                tma_load_2d(sW + s * kPWBytes, &tm_w, &full[s], kb * kPK, m0);
-                tma_load_2d(sX + s * kPXBytes, &tm_x, &full[s], kb * kPK, x_first);
+                tma_load_2d(sW + s * kPWBytes, tm_w, &full[s], kb * kPK, m0);
+                tma_load_2d(sX + s * kPXBytes, tm_x, &full[s], kb * kPK, x_first);
                 issued = kb + 1;
             }
             if (*abort_flag) {
@@ -242,10 +258,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int h = (warp - 2) >> 2;
         const int r = sub * 32 + lane;
         const int64_t row = static_cast<int64_t>(m0) + r;
-        const bool row_ok = row < a.n_out;
+        const bool row_ok = row < L.n_out;
         const float al = row_ok ? (mode ? alpha[row] : alpha[0]) : 0.0f;
         const uint32_t neg_al = pack_bf16x2(-al, -al);  // -alpha_b in both halves
-        const int64_t bpr = a.n_in / 8;
+        const int64_t bpr = L.n_in / 8;
         const uint8_t *brow = bits + (row_ok ? row : 0) * bpr;
         const uint32_t rebuilt0 = mapa_rank(smem_u32(rebuilt), 0);  // the even CTA's barriers
         const uint32_t a_lane = tmem + (static_cast<uint32_t>(sub * 32) << 16) + kPAccCols;
@@ -254,7 +270,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint2 v = make_uint2(0u, 0u);
             const int64_t c0 = static_cast<int64_t>(kb) * 8;  // first packed byte of the block
             if (row_ok && kb < nkb) {
-                if (a.bits_vec8 && c0 + 8 <= bpr) {
+                if (L.bits_vec8 && c0 + 8 <= bpr) {
                     v = __ldg(reinterpret_cast<const uint2 *>(brow + c0));
                 } else {
                     for (int c = 0; c < 8; ++c)
@@ -309,7 +325,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (__all_sync(0xFFFFFFFFu, got)) {
                 tc_fence_after();
                 const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sub * 32) << 16);
-                uint16_t *ycol = a.y + row;
+                uint16_t *ycol = L.y + row;
 #pragma unroll 1
                 for (int c0 = h * (kPN / 2); c0 < (h + 1) * (kPN / 2); c0 += 32) {
                     if (c0 >= count) break;  // warp-uniform
@@ -323,7 +339,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                                 const int64_t t = kGrouped ? static_cast<int64_t>(a.perm[n0 + c0 + i])
                                                            : static_cast<int64_t>(n0) + c0 + i;
                                 __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[i]));
-                                ycol[t * a.n_out] = *reinterpret_cast<uint16_t *>(&hv);
+                                ycol[t * L.n_out] = *reinterpret_cast<uint16_t *>(&hv);
                             }
                         }
                     }
@@ -360,8 +376,8 @@ int64_t prefill_pair_tiles(int64_t m, int64_t n_out) {
 namespace {
 
 template <bool kGrouped>
-cudaError_t launch_pair(const PairArgs &a, const void *w_base, const void *x, int64_t x_rows, int64_t pairs,
-                        const DevCtx &ctx, cudaStream_t stream) {
+cudaError_t launch_pair(const PairMaps &maps, const PairArgs &a, int64_t pairs, const DevCtx &ctx,
+                        cudaStream_t stream) {
     static bool attr_set[128] = {false};
     if (ctx.device < 128 && !attr_set[ctx.device]) {
         cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<kGrouped>,
@@ -369,12 +385,7 @@ cudaError_t launch_pair(const PairArgs &a, const void *w_base, const void *x, in
         if (e != cudaSuccess) return e;
         attr_set[ctx.device] = true;
     }
-    CUtensorMap tm_w, tm_x;
-    if (!encode_tensor_map_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, a.n_in, a.n_out, a.n_in * 2, kPK, kPM,
-                              CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, a.n_in, x_rows, a.n_in * 2, kPK, kPN / 2,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    if (pairs < 1) return cudaSuccess;
     if (2 * pairs > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
@@ -388,43 +399,79 @@ cudaError_t launch_pair(const PairArgs &a, const void *w_base, const void *x, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<kGrouped>, tm_w, tm_x, a);
+    return cudaLaunchKernelEx(&cfg, prefill_pair_kernel<kGrouped>, maps, a);
 }
 
-void fill_pair_common(PairArgs &a, int64_t m, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx) {
-    a.y = static_cast<uint16_t *>(y);
-    a.m = m;
-    a.n_out = n_out;
-    a.n_in = n_in;
-    a.num_kb = static_cast<int32_t>((n_in + kPK - 1) / kPK);
-    a.row_tiles = static_cast<int32_t>((n_out + 2 * kPM - 1) / (2 * kPM));
-    a.status = ctx.status;
-    a.wait_ns = ctx.wait_ns;
+// Shape, maps and tiling of linear i of a launch; returns false if a tensor map cannot be encoded.
+bool fill_linear(PairMaps &maps, PairArgs &a, int i, const void *x, int64_t x_rows, const void *w_base,
+                 const uint8_t *bits, const float *alpha, int32_t mode, int64_t m, int64_t n_out, int64_t n_in,
+                 void *y, int32_t first_pair) {
+    PairLinear &L = a.lin[i];
+    L.bits = bits;
+    L.alpha = alpha;
+    L.y = static_cast<uint16_t *>(y);
+    L.m = m;
+    L.n_out = n_out;
+    L.n_in = n_in;
+    L.mode = mode;
+    L.num_kb = static_cast<int32_t>((n_in + kPK - 1) / kPK);
+    L.row_tiles = static_cast<int32_t>((n_out + 2 * kPM - 1) / (2 * kPM));
+    L.tok_tiles = static_cast<int32_t>((m + kPN - 1) / kPN);
+    L.group = L.tok_tiles < 8 ? L.tok_tiles : 8;
+    L.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
+    L.first_pair = first_pair;
+    return encode_tensor_map_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kPK,
+                                kPM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode_tensor_map_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, x_rows, n_in * 2, kPK,
+                                kPN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
 
+bool prefill_pair_multi_supported(const BatchItem *items, int n, const DevCtx &ctx) {
+    if (n < 1 || n > kPMaxLinears) return false;
+    for (int i = 0; i < n; ++i)
+        if (!prefill_pair_supported(items[i].m, items[i].n_out, items[i].n_in, ctx)) return false;
+    return true;
+}
+
+cudaError_t launch_prefill_pair_multi(const BatchItem *items, int n, const DevCtx &ctx, cudaStream_t stream) {
+    if (!prefill_pair_multi_supported(items, n, ctx)) return cudaErrorNotSupported;
+    PairMaps maps;
+    PairArgs a = {};
+    a.n_lin = n;
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
+    int64_t pairs = 0;
+    for (int i = 0; i < n; ++i) {
+        const BatchItem &it = items[i];
+        if (pairs > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
+        if (!fill_linear(maps, a, i, it.x, it.m, it.w_base, it.bits, it.alpha, it.alpha_mode, it.m, it.n_out, it.n_in,
+                         it.y, static_cast<int32_t>(pairs)))
+            return cudaErrorInvalidValue;
+        pairs += prefill_pair_tiles(it.m, it.n_out);
+    }
+    return launch_pair<false>(maps, a, pairs, ctx, stream);
+}
+
 cudaError_t launch_prefill_pair(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                                 int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                                 cudaStream_t stream) {
-    if (!prefill_pair_supported(m, n_out, n_in, ctx)) return cudaErrorNotSupported;
-    PairArgs a = {};
-    fill_pair_common(a, m, n_out, n_in, y, ctx);
-    a.bits = bits;
-    a.alpha = alpha;
-    a.mode = alpha_mode;
-    a.tok_tiles = static_cast<int32_t>((m + kPN - 1) / kPN);
-    a.group = a.tok_tiles < 8 ? a.tok_tiles : 8;
-    a.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
-    return launch_pair<false>(a, w_base, x, m, static_cast<int64_t>(a.row_tiles) * a.tok_tiles, ctx, stream);
+    const BatchItem it{x, w_base, bits, alpha, y, m, n_out, n_in, alpha_mode};
+    return launch_prefill_pair_multi(&it, 1, ctx, stream);
 }
 
 cudaError_t launch_prefill_pair_grouped(const void *x_sorted, int64_t m, const void *w_base,
                                         const GroupedVariants &vars, int64_t n_out, int64_t n_in, void *y,
                                         const GroupTable &tab, const DevCtx &ctx, cudaStream_t stream) {
     if (!prefill_pair_supported(m, n_out, n_in, ctx) || vars.count > kPMaxVariants) return cudaErrorNotSupported;
+    PairMaps maps;
     PairArgs a = {};
-    fill_pair_common(a, m, n_out, n_in, y, ctx);
+    a.n_lin = 1;
+    a.status = ctx.status;
+    a.wait_ns = ctx.wait_ns;
+    if (!fill_linear(maps, a, 0, x_sorted, m, w_base, nullptr, nullptr, 0, m, n_out, n_in, y, 0))
+        return cudaErrorInvalidValue;
     bool vec8 = (n_in / 8) % 8 == 0;
     for (int v = 0; v < vars.count; ++v) {
         a.vbits[v] = vars.bits[v];
@@ -432,12 +479,12 @@ cudaError_t launch_prefill_pair_grouped(const void *x_sorted, int64_t m, const v
         a.vmode[v] = vars.mode[v];
         vec8 = vec8 && (reinterpret_cast<uintptr_t>(vars.bits[v]) & 7) == 0;
     }
-    a.bits_vec8 = vec8 ? 1 : 0;
+    a.lin[0].bits_vec8 = vec8 ? 1 : 0;
     a.tiles = tab.tiles;
     a.n_tiles = tab.n_tiles;
     a.perm = tab.perm;
     a.max_slots = tab.max_slots;
-    return launch_pair<true>(a, w_base, x_sorted, m, static_cast<int64_t>(a.row_tiles) * tab.max_slots, ctx, stream);
+    return launch_pair<true>(maps, a, static_cast<int64_t>(a.lin[0].row_tiles) * tab.max_slots, ctx, stream);
 }
 
 }  // namespace bd

@@ -208,8 +208,13 @@ int32_t bd_linear(const void *x, int64_t m, const void *w_base,
  * step of one 64-row block -- are split evenly over the resident CTAs.
  * Either way a row block's fp32 partials are summed in a fixed order, so
  * results are deterministic; they may differ from bd_linear's in the last
- * bits of fp32 rounding (another split of K).  Every other problem, and a
- * group that would hold a single problem, runs as bd_linear.
+ * bits of fp32 rounding (another split of K).  Problems with m > 64 (the
+ * tensor-core path) are launched together on the CTA-pair kernel, up to
+ * BD_LINEAR_BATCH_PER_LAUNCH per launch, when their 256 x 256 tiles together
+ * fill the GPU at least once -- a layer's q, k and v at prefill sizes, or gate
+ * and up; such a problem computes what bd_linear computes on that kernel
+ * (without a K split).  Every other problem, and a group that would hold a
+ * single problem, runs as bd_linear.
  *
  *   descs      host array [n] of bd_linear_desc (read during the call only;
  *              `reserved` must be 0)

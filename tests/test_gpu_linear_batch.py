@@ -246,3 +246,51 @@ def test_workspace_errors():
     assert bd.bd_linear_batch_workspace_size(bd.linear_descs(
         [(cases[0].x, cases[0].w_base, cases[0].bits, cases[0].alpha, 0, ys[0])])) == 0
     assert bd.bd_linear_batch_workspace_size((bd.LinearDesc * 0)()) == 0
+
+
+# Tensor-core problems launched together on the pair kernel: ragged rows (vs 256), ragged token
+# tiles, different K per linear, several linears per pair wave; each batch has at least 76 pair
+# tiles (256 W rows x 256 tokens), so that together they fill the 152 SMs and share one launch.
+PAIR_BATCHES = {
+    "qkv_like": [(4096, 1024, 1000), (1024, 1024, 1000), (1024, 1024, 1000)],
+    "ragged": [(1000, 640, 300), (2570, 4096, 777), (3000, 192, 300), (130, 520, 2048)],
+    "gate_up_like": [(3584, 1024, 513), (3584, 1024, 513)],
+}
+
+
+@pytest.mark.parametrize("name", list(PAIR_BATCHES))
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tensor_core_problems_on_the_pair_kernel(name, mode):
+    cases = make_cases(PAIR_BATCHES[name], seed0=700, mode=mode)
+    ys, ws = run_batch(cases)
+    check_all(cases, ys, f"pair batch {name} mode={mode}")
+    assert_reusable(cases, ys, ws, f"pair batch {name}")
+    # the same problems one by one on the pair kernel: identical bits
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, 2):
+        for c, y in zip(cases, ys):
+            y1 = torch.empty_like(y)
+            bd.bd_linear(c.x, c.w_base, c.bits, c.alpha, c.mode, y1)
+            torch.cuda.synchronize()
+            assert torch.equal(y1, y), f"{name}: {c.n_out}x{c.n_in} m={c.m} differs from bd_linear"
+
+
+def test_llama3_8b_layer_prefill_batches_full_size():
+    """A stack layer's q/k/v and gate/up at 2048 tokens, each group in one bd_linear_batch call (one
+    pair-kernel launch each), sampled outputs against the oracle."""
+    c = workloads.LLAMA3_8B_STACK
+    mats = dict((n, (a, b)) for n, a, b in c["matrices"])
+    for group in (("q", "k", "v"), ("gate", "up")):
+        cases = [LinearCase(mats[g][0], mats[g][1], 2048, c["sigma"], c["b"], c["mode"],
+                            seed=workloads.matrix_seed(c["seed"], 900 + j)) for j, g in enumerate(group)]
+        x = cases[0].x
+        for cs in cases[1:]:  # the group shares its input, as in a layer
+            cs.x, cs.x_h = x, cases[0].x_h
+        ys, _ = run_batch(cases)
+        torch.cuda.synchronize()
+        assert bd.bd_get_device_status() == bd.BD_OK
+        for g, cs, y in zip(group, cases, ys):
+            ts, js = sample_outputs(cs.m, cs.n_out, 800, seed=cs.n_out)
+            y_ref, mag = cs.reference_sampled(ts, js)
+            assert_y_close(y_host(y)[ts, js], y_ref, mag, f"{g} m=2048")
+        del cases, ys
+        torch.cuda.empty_cache()
