@@ -802,7 +802,7 @@ def run_ours(args, ws, rank, local):
 # Sources whose change invalidates a stored traffic figure, by phase bound.
 KERNEL_SOURCES = {"hbm": ("decode_tma.cu", "decode_batch.cu", "decode_stage.cuh", "grouped_decode.cu", "grouped.cu",
                           "compress.cu", "api.cu"),
-                  "tensor": ("prefill.cu", "grouped.cu", "api.cu")}
+                  "tensor": ("prefill.cu", "prefill_pair.cu", "grouped.cu", "api.cu")}
 
 
 def traffic_path(workload: str) -> str:

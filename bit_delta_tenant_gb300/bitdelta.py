@@ -16,6 +16,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libbitdelta.so")
+# the bounds-checked build (``build.build(debug=True)``): load it with load_library(LIB_DEBUG_PATH)
+LIB_DEBUG_PATH = os.path.join(_HERE, "lib", "libbitdelta_debug.so")
 
 BD_OK = 0
 BD_ERR_INVALID_ARG = 1
@@ -26,6 +28,7 @@ BD_ERR_CUDA = 5
 BD_ERR_DEVICE_TIMEOUT = 6
 BD_ERR_BAD_VARIANT_ID = 7
 BD_ERR_NO_SPACE = 8
+BD_ERR_DEVICE_BOUNDS = 9
 BD_ALPHA_SCALAR = 0
 BD_ALPHA_PER_ROW = 1
 BD_MAX_VARIANTS = 64
@@ -80,6 +83,7 @@ def load_library(path: str | None = None):
         lib = ctypes.CDLL(p)
         V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         lib.bd_version.restype = I32
+        lib.bd_build_flags.restype = I32
         lib.bd_status_string.argtypes = [I32]
         lib.bd_status_string.restype = ctypes.c_char_p
         lib.bd_set_wait_limit_ns.argtypes = [I64]
@@ -156,6 +160,10 @@ def _check(rc: int, where: str) -> None:
 
 def bd_version() -> int:
     return int(load_library().bd_version())
+
+
+def bd_build_flags() -> int:
+    return int(load_library().bd_build_flags())
 
 
 def bd_status_string(status: int) -> str:

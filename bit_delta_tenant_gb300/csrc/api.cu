@@ -135,6 +135,14 @@ bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
 
 BD_API int32_t bd_version(void) { return 100; }
 
+BD_API int32_t bd_build_flags(void) {
+#ifdef BD_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 BD_API const char *bd_status_string(int32_t status) {
     switch (status) {
         case BD_OK: return "ok";
@@ -146,6 +154,7 @@ BD_API const char *bd_status_string(int32_t status) {
         case BD_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
         case BD_ERR_BAD_VARIANT_ID: return "variant id outside [0, n_variants)";
         case BD_ERR_NO_SPACE: return "delta cache: no evictable delta leaves room for the request";
+        case BD_ERR_DEVICE_BOUNDS: return "bounds-checked build: a device index failed its check (access skipped)";
         default: return "unknown status";
     }
 }
@@ -182,6 +191,7 @@ BD_API int32_t bd_get_device_status(void *stream) {
     if (cudaMemcpyFromSymbol(&word, g_bd_status_word, sizeof(word)) != cudaSuccess) return BD_ERR_CUDA;
     const unsigned zero = 0;
     if (word != 0 && cudaMemcpyToSymbol(g_bd_status_word, &zero, sizeof(zero)) != cudaSuccess) return BD_ERR_CUDA;
+    if (word & bd::kDevBounds) return BD_ERR_DEVICE_BOUNDS;
     if (word & bd::kDevTimeout) return BD_ERR_DEVICE_TIMEOUT;
     if (word & bd::kDevBadVariant) return BD_ERR_BAD_VARIANT_ID;
     return BD_OK;

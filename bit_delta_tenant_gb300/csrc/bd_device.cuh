@@ -28,6 +28,19 @@ __device__ __forceinline__ void flag_status(unsigned *status, unsigned bit) {
     if (status) atomicOr(status, bit);
 }
 
+// Bounds check of a global index.  In the bounds-checked build (-DBD_DEBUG) a
+// failed check records kDevBounds in the status word and the caller skips the
+// access (never a trap: the context stays usable and the host reads the word);
+// in the release build the check compiles away.
+#ifdef BD_DEBUG
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned *status) {
+    if (!ok) flag_status(status, kDevBounds);
+    return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, unsigned *) { return true; }
+#endif
+
 // ---- bf16 <-> fp32 on raw bits ------------------------------------------------
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t pair) { return __uint_as_float(pair << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }

@@ -15,6 +15,7 @@ namespace bd {
 // and cleared by the host).
 constexpr unsigned kDevTimeout = 1u;
 constexpr unsigned kDevBadVariant = 2u;
+constexpr unsigned kDevBounds = 4u;  // bounds-checked build: an index failed its check (access skipped)
 
 // Per-launch context every kernel receives: where to record device-side
 // errors, and the wall-clock limit of bounded waits.

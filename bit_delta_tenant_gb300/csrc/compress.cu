@@ -43,6 +43,8 @@ struct CompressArgs {
     double count;      // elements per row: alpha = sum / count
     int64_t row_chunks;
     int64_t segs;
+    int64_t rows;        // alpha entries (1 or n_out); bits hold rows * row_chunks bytes
+    unsigned *status;    // bounds-checked build: where a failed index check is recorded
     int32_t test_stall;  // ring form: the first consumer wait is on a barrier nothing completes (tests)
 };
 
@@ -192,7 +194,8 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
                 if (c < n) {
                     float sum;
                     const uint32_t byte = chunk_signs(sb[cl], sf[cl], sum);
-                    bits[c] = static_cast<uint8_t>(byte);
+                    if (in_bounds(row < a.rows && first + c < a.row_chunks, a.status))
+                        bits[c] = static_cast<uint8_t>(byte);
 #pragma unroll
                     for (int hh = 0; hh < kSlotsPerSeg; ++hh)
                         if (h == hh) cs[hh * kChunksPerSlotThread + uu] = sum;
@@ -226,10 +229,12 @@ __global__ void __launch_bounds__(kPass1Threads, 2)
             double s = 0.0;
 #pragma unroll
             for (int w = 0; w < kCompressThreads / 32; ++w) s += ws[w];
-            if (a.segs == 1)
-                a.alpha[row] = static_cast<float>(s / a.count);  // the row's only partial: no second pass
-            else
+            if (a.segs == 1) {
+                if (in_bounds(row < a.rows, a.status))
+                    a.alpha[row] = static_cast<float>(s / a.count);  // the row's only partial: no second pass
+            } else if (in_bounds(sg < a.rows * a.segs, a.status)) {
                 a.partials[sg] = s;
+            }
         }
         if (*abort_flag) break;
     }
@@ -267,7 +272,8 @@ __device__ __forceinline__ void compress_segment(const CompressArgs &a, int64_t 
         cs[u] = 0.0f;
         if (c < n) {
             float sum;
-            bits[c] = static_cast<uint8_t>(chunk_signs(b[u], f[u], sum));
+            const uint32_t byte = chunk_signs(b[u], f[u], sum);
+            if (in_bounds(row < a.rows && first + c < a.row_chunks, a.status)) bits[c] = static_cast<uint8_t>(byte);
             cs[u] = sum;
         }
     }
@@ -288,10 +294,11 @@ __device__ __forceinline__ void compress_segment(const CompressArgs &a, int64_t 
         double s = 0.0;
 #pragma unroll
         for (int w = 0; w < kCompressThreads / 32; ++w) s += warp_sum[w];
-        if (a.segs == 1)
-            a.alpha[row] = static_cast<float>(s / a.count);
-        else
+        if (a.segs == 1) {
+            if (in_bounds(row < a.rows, a.status)) a.alpha[row] = static_cast<float>(s / a.count);
+        } else if (in_bounds(sg < a.rows * a.segs, a.status)) {
             a.partials[sg] = s;
+        }
     }
 }
 
@@ -418,6 +425,8 @@ cudaError_t launch_compress(const void *w_base, const void *w_ft, int64_t n_out,
     a.count = static_cast<double>(g.row_chunks) * 8.0;
     a.row_chunks = g.row_chunks;
     a.segs = g.segs;
+    a.rows = g.rows;
+    a.status = ctx.status;
     a.test_stall = ctx.test_stall ? 1 : 0;
     const int64_t n_segs = g.rows * g.segs;
     static bool attr_set[128] = {false};
@@ -486,6 +495,8 @@ cudaError_t launch_compress_batch(const CompressItem *items, int n, const DevCtx
         a.count = static_cast<double>(g.row_chunks) * 8.0;
         a.row_chunks = g.row_chunks;
         a.segs = g.segs;
+        a.rows = g.rows;
+        a.status = ctx.status;
         a.test_stall = 0;  // the direct form has no pipeline waits
         a1.first_block[i] = blocks1;
         blocks1 += g.rows * g.segs;

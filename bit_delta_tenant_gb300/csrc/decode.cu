@@ -53,6 +53,7 @@ struct DecodeArgs {
     int32_t cluster;   // CTAs per cluster along K
     int32_t x_stride;  // bytes per token row of the staged slice
     int32_t bits16;    // packed rows are 16-byte aligned in kStep units
+    unsigned *status;  // bounds-checked build: where a failed index check is recorded
 };
 
 __device__ __forceinline__ uint32_t byte_of(uint32_t word, int t) { return (word >> (8 * t)) & 0xFFu; }
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeArgs a) {
         const int tok = i / share;
         const int lr = rank * share + (i - tok * share);
         const int64_t row = row_block * kRowsPerCta + lr;
-        if (lr < kRowsPerCta && row < a.n_out) {
+        if (lr < kRowsPerCta && row < a.n_out && in_bounds(tok < a.m, a.status)) {
             float s = 0.0f;
             for (int q = 0; q < a.cluster; ++q) {
                 const float *rr = cluster.map_shared_rank(red, q);
@@ -281,6 +282,7 @@ cudaError_t launch_decode(const void *x, int64_t m, const void *w_base, const ui
     a.cluster = p.cluster;
     a.x_stride = p.x_stride;
     a.bits16 = ((n_in % 128 == 0) && ((reinterpret_cast<uintptr_t>(bits) & 15) == 0)) ? 1 : 0;
+    a.status = ctx.status;
     switch (p.nt) {
         case 1: return launch_nt<1>(a, p, ctx, stream);
         case 2: return launch_nt<2>(a, p, ctx, stream);

@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float sv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    if (row0 + lr + k < P.n_out) {
+                    if (row0 + lr + k < P.n_out && in_bounds(tok < P.m, a.status)) {
                         const __nv_bfloat16 h = __float2bfloat16_rn(sv[k]);
                         P.y[tok * P.n_out + row0 + lr + k] = *reinterpret_cast<const uint16_t *>(&h);
                     }
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int u = 0; u < kVec; ++u) {
                     const int e = lane + 32 * u;
-                    if (e < n4)
+                    if (e < n4 && in_bounds(part_i < a.parts_max, a.status))
                         reinterpret_cast<float4 *>(slots + part_i * kRed)[e] = reinterpret_cast<const float4 *>(rb)[e];
                 }
                 __syncwarp();

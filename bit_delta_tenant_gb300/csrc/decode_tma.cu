@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(32 * (2 * RG + 1), NT <= 2 && RG <= 4 ? 2 : 1)
         float s = 0.0f;
         for (int q = 0; q < a.cluster; ++q)
             s += q == rank ? red[tok * rows + lr] : inbox[(q * MP + tok) * share + lrl];
-        if (row < P.n_out) {
+        if (row < P.n_out && in_bounds(tok < P.m, a.status)) {
             __nv_bfloat16 h = __float2bfloat16_rn(s);
             P.y[static_cast<int64_t>(tok) * P.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
         }

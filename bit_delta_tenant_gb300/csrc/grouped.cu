@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) group_sort_kernel(SortArgs a)
         const unsigned peers = __match_any_sync(0xFFFFFFFFu, id);
         if (id >= 0) {
             const int32_t pos = cnt[warp][id] + __popc(peers & lt_mask);
-            a.perm[pos] = static_cast<int32_t>(t);
+            if (in_bounds(pos >= 0 && pos < a.m, a.status)) a.perm[pos] = static_cast<int32_t>(t);
         }
         __syncwarp();
         if (id >= 0 && (peers & lt_mask) == 0) cnt[warp][id] += __popc(peers);
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kSortThreads, 1) group_sort_kernel(SortArgs a)
 
 // xs[r] = x[map[r]] (a zero row where map[r] < 0), rows r < *n_rows.
 __global__ void group_gather_kernel(const uint4 *x, int64_t vec_per_row, const int32_t *map, const int32_t *n_rows,
-                                    int64_t max_rows, uint4 *xs) {
+                                    int64_t max_rows, uint4 *xs, unsigned *status) {
     const int64_t rows = *n_rows;
     const int64_t total = max_rows * vec_per_row;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -181,6 +181,7 @@ __global__ void group_gather_kernel(const uint4 *x, int64_t vec_per_row, const i
         if (r >= rows) continue;
         const int64_t c = i - r * vec_per_row;
         const int32_t src = map[r];
+        if (!in_bounds(src < max_rows, status)) continue;  // map rows name tokens of x ([max_rows] rows)
         xs[i] = src >= 0 ? x[static_cast<int64_t>(src) * vec_per_row + c] : make_uint4(0, 0, 0, 0);
     }
 }
@@ -220,7 +221,7 @@ cudaError_t launch_grouped(const void *x, const int32_t *ids, int64_t m, const v
     if (nblk > 8 * static_cast<int64_t>(ctx.num_sms)) nblk = 8 * static_cast<int64_t>(ctx.num_sms);
     const int blocks = static_cast<int>(nblk);
     group_gather_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(static_cast<const uint4 *>(x), vec, s.perm,
-                                                                     s.seg + vars.count, m, xs);
+                                                                     s.seg + vars.count, m, xs, ctx.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 

@@ -372,7 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float s = SIGN ? a.ybase[static_cast<int64_t>(tok) * a.n_out + row] : 0.0f;
             for (int q = 0; q < a.cluster; ++q) s += cluster.map_shared_rank(red, q)[tok * kRows + lr];
             __nv_bfloat16 h = __float2bfloat16_rn(s);
-            a.y[static_cast<int64_t>(a.perm[tok]) * a.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
+            const int64_t t = in_bounds(tok < a.m, a.status) ? a.perm[tok] : -1;
+            if (in_bounds(t >= 0 && t < a.m, a.status))
+                a.y[t * a.n_out + row] = *reinterpret_cast<uint16_t *>(&h);
         }
     }
     cluster.sync();

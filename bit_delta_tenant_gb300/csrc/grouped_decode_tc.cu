@@ -338,7 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdec_tc_kernel(const __grid_const
                 float s = 0.0f;
                 for (int q = 0; q < a.cluster; ++q) s += cluster.map_shared_rank(red, q)[tok * kBM + lr];
                 __nv_bfloat16 hv = __float2bfloat16_rn(s);
-                a.y[static_cast<int64_t>(a.perm[tok]) * a.n_out + grow] = *reinterpret_cast<uint16_t *>(&hv);
+                const int64_t t = in_bounds(tok < a.m, a.status) ? a.perm[tok] : -1;
+                if (in_bounds(t >= 0 && t < a.m, a.status))
+                    a.y[t * a.n_out + grow] = *reinterpret_cast<uint16_t *>(&hv);
             }
         }
     }

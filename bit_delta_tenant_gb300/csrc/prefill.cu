@@ -381,9 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (row_ok) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            if (c0 + i < count) {
+                            if (c0 + i < count && in_bounds(n0 + c0 + i < a.m, a.status)) {
                                 const int64_t t = kGrouped ? static_cast<int64_t>(a.perm[n0 + c0 + i])
                                                            : static_cast<int64_t>(n0) + c0 + i;
+                                if (!in_bounds(t >= 0 && t < a.m, a.status)) continue;
                                 if (!kGrouped && a.y32 != nullptr) {
                                     a.y32[t * a.n_out + row] = __uint_as_float(v[i]);
                                 } else {
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = rank * share + threadIdx.x; e < e1; e += kThreads) {
                 const int tok = e / kBM, rr = e - tok * kBM;
                 const int64_t orow = static_cast<int64_t>(m0) + rr;
-                if (orow < a.n_out) {
+                if (orow < a.n_out && in_bounds(n0 + tok < a.m, a.status)) {
                     float sum = 0.0f;
                     for (int q = 0; q < a.ksplit; ++q) sum += cluster.map_shared_rank(red, q)[e];
                     if (a.y32 != nullptr) {
@@ -531,11 +532,11 @@ cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const u
                            int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                            cudaStream_t stream) {
     // CTA pairs (256 x 256 tiles, half the activation traffic per SM) once their
-    // CTAs fill the SMs at least once; below that the single-CTA tiles, which can
-    // split K over a cluster to fill them.
+    // CTAs fill at least three quarters of the SMs; below that the single-CTA
+    // tiles, which can split K over a cluster to fill them.
     const int64_t forced = option_value(BD_OPT_PREFILL_KERNEL);
     const bool pair = forced == 2 || (forced == 0 && m > 64 &&
-                                      2 * prefill_pair_tiles(m, n_out) >= static_cast<int64_t>(ctx.num_sms));
+                                      8 * prefill_pair_tiles(m, n_out) >= 3 * static_cast<int64_t>(ctx.num_sms));
     if (pair && prefill_pair_supported(m, n_out, n_in, ctx))
         return launch_prefill_pair(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
     if (m <= 64)

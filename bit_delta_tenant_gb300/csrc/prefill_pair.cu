@@ -335,9 +335,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (row_ok) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            if (c0 + i < count) {
+                            if (c0 + i < count && in_bounds(n0 + c0 + i < L.m, a.status)) {
                                 const int64_t t = kGrouped ? static_cast<int64_t>(a.perm[n0 + c0 + i])
                                                            : static_cast<int64_t>(n0) + c0 + i;
+                                if (!in_bounds(t >= 0 && t < L.m, a.status)) continue;
                                 __nv_bfloat16 hv = __float2bfloat16_rn(__uint_as_float(v[i]));
                                 ycol[t * L.n_out] = *reinterpret_cast<uint16_t *>(&hv);
                             }

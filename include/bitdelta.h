@@ -60,7 +60,9 @@ typedef enum bd_status {
     BD_ERR_CUDA = 5,              /* a CUDA runtime call failed                 */
     BD_ERR_DEVICE_TIMEOUT = 6,    /* a bounded device-side wait ran out         */
     BD_ERR_BAD_VARIANT_ID = 7,    /* a variant id outside [0, n_variants)       */
-    BD_ERR_NO_SPACE = 8           /* delta cache: nothing evictable leaves room  */
+    BD_ERR_NO_SPACE = 8,          /* delta cache: nothing evictable leaves room  */
+    BD_ERR_DEVICE_BOUNDS = 9      /* bounds-checked build only: a device index
+                                     failed its check and the access was skipped */
 } bd_status;
 
 /* How alpha is stored ([math]: one per matrix; [infra]: one per output row). */
@@ -392,8 +394,9 @@ int32_t bd_cache_is_resident(bd_cache *cache, int32_t variant);
 const char *bd_status_string(int32_t status);
 
 /* Synchronises `stream`, then reads and clears the device status word of the
- * current device: BD_OK, BD_ERR_DEVICE_TIMEOUT or BD_ERR_BAD_VARIANT_ID (the
- * first recorded, timeouts first).  BD_ERR_CUDA if the sync itself fails. */
+ * current device: BD_OK, BD_ERR_DEVICE_BOUNDS (bounds-checked build only),
+ * BD_ERR_DEVICE_TIMEOUT or BD_ERR_BAD_VARIANT_ID (in that order of precedence).
+ * BD_ERR_CUDA if the sync itself fails. */
 int32_t bd_get_device_status(void *stream);
 
 /* Debug knob: wall-clock limit, in nanoseconds, of every bounded device-side
@@ -466,6 +469,13 @@ int32_t bd_set_weight_prefetch(int32_t enable);
 #define BD_OPT_TEST_STALL 6
 #define BD_OPT_PREFILL_KERNEL 7
 int64_t bd_set_option(int32_t option, int64_t value);
+
+/* Build flags of the loaded library: bit 0 set in the bounds-checked build
+ * (compiled with BD_DEBUG: every kernel checks the indices of its global
+ * accesses against the extents it was given, skips an access that fails and
+ * records BD_ERR_DEVICE_BOUNDS in the device status word; a stand-in for a
+ * memory checker, slower than the release build and not for measurement). */
+int32_t bd_build_flags(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t bd_version(void);
