@@ -1213,7 +1213,8 @@ def run_kernel_case(args):
 
     --kernel-case linear:N_OUTxN_IN:M[:path], compress:N_OUTxN_IN[:mode],
                   batch:N_OUTxN_IN:M:COUNT (COUNT linears per bd_linear_batch call),
-                  grouped:N_OUTxN_IN:M:V (V variants, uniform ids), reconstruct:N_OUTxN_IN
+                  grouped:N_OUTxN_IN:M:V[:zipf] (V variants, uniform ids or Zipf(1.1) segments),
+                  reconstruct:N_OUTxN_IN
                   (W_eff materialised), reconstruct_mm:N_OUTxN_IN:M (W_eff + a cuBLAS matmul) or
                   cache_load:N_OUTxN_IN (a delta's cold load through the delta cache)
     Rotates over enough copies of the weights that the working set exceeds L2.
@@ -1346,7 +1347,8 @@ def run_kernel_case(args):
                 bits = torch.randint(0, 256, (n_out, n_in // 8), generator=g, device=dev, dtype=torch.uint8)
                 vs.append((bits, torch.full((1,), 1e-3, dtype=torch.float32, device=dev)))
             packed.append(vs)
-        ids = torch.from_numpy(synth.uniform_ids(m, nv, 3)).to(dev)
+        zipf = len(parts) > 4 and parts[4] == "zipf"  # Zipf(1.1) segments (the 14-variant prefill batch's mix)
+        ids = torch.from_numpy(synth.zipf_ids(m, nv, 1.1, 3) if zipf else synth.uniform_ids(m, nv, 3)).to(dev)
         x = synth.activations(m, n_in, 7, dev)
         y = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
         gws = torch.empty((bd.bd_linear_grouped_workspace_size(m, nv, n_out, n_in),), dtype=torch.uint8, device=dev)
