@@ -242,12 +242,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     aaddr[s][kk] = tmem + kPAccCols + s * (kPK / 2) + kk * 8;
                 }
             bool ok = true;
-            for (int kb0 = 0; kb0 < nkb && ok; kb0 += kPStages) {
+            for (int ring = 0; ring < nkb && ok; ring += kPStages) {  // a ring's worth of K blocks at a time
 #pragma unroll
                 for (int s = 0; s < kPStages; ++s) {
-                    const int kb = kb0 + s;
+                    const int kb = ring + s;
                     if (kb >= nkb) break;
-                    const uint32_t ph = (kb0 / kPStages) & 1;
+                    const uint32_t ph = (ring / kPStages) & 1;
                     if (!mbar_wait(&rebuilt[s], ph, a.wait_ns, abort_flag)) {
                         give_up_p(abort_flag, a.status);
                         ok = false;
