@@ -44,6 +44,7 @@ BD_OPT_BATCH_SINGLE = 4
 BD_OPT_BATCH_GRID = 5
 BD_OPT_TEST_STALL = 6
 BD_OPT_PREFILL_KERNEL = 7
+BD_OPT_PAIR_RING = 8
 
 _lock = threading.Lock()
 _lib = None

@@ -26,7 +26,7 @@ int g_num_sms[kMaxDevices] = {0};
 std::atomic<int64_t> g_wait_ns{-1};
 std::atomic<int32_t> g_linear_path{0};
 std::atomic<int32_t> g_weight_prefetch{0};
-constexpr int kNumOptions = BD_OPT_PREFILL_KERNEL + 1;
+constexpr int kNumOptions = BD_OPT_PAIR_RING + 1;
 std::atomic<int64_t> g_options[kNumOptions] = {};
 
 int64_t wait_limit_ns() {
@@ -49,6 +49,7 @@ int64_t option_max(int32_t option) {
         case BD_OPT_BATCH_GRID: return 0x7FFFFFFFLL;
         case BD_OPT_TEST_STALL: return 1;
         case BD_OPT_PREFILL_KERNEL: return 2;
+        case BD_OPT_PAIR_RING: return 2;
         default: return -1;
     }
 }

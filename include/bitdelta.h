@@ -460,7 +460,11 @@ int32_t bd_set_weight_prefetch(int32_t enable);
  *                         kernel takes its give-up path (tests of failure
  *                         detection; results are then undefined and
  *                         bd_get_device_status reports
- *                         BD_ERR_DEVICE_TIMEOUT) */
+ *                         BD_ERR_DEVICE_TIMEOUT)
+ *   BD_OPT_PAIR_RING      shape of the CTA-pair tensor-core kernel: 0
+ *                         automatic (by K); 1 a 5-deep K-block ring with
+ *                         the whole output tile staged; 2 a 6-deep ring
+ *                         with the tile staged in two halves */
 #define BD_OPT_COMPRESS_FORM 1
 #define BD_OPT_GROUPED_PATH 2
 #define BD_OPT_BATCH_KERNEL 3
@@ -468,6 +472,7 @@ int32_t bd_set_weight_prefetch(int32_t enable);
 #define BD_OPT_BATCH_GRID 5
 #define BD_OPT_TEST_STALL 6
 #define BD_OPT_PREFILL_KERNEL 7
+#define BD_OPT_PAIR_RING 8
 int64_t bd_set_option(int32_t option, int64_t value);
 
 /* Build flags of the loaded library: bit 0 set in the bounds-checked build

@@ -203,6 +203,21 @@ def test_knobs_round_trip(lib):
     assert bd.bd_set_weight_prefetch(w) == 1
 
 
+@pytest.mark.parametrize("option,top", [(bd.BD_OPT_COMPRESS_FORM, 1), (bd.BD_OPT_GROUPED_PATH, 4),
+                                        (bd.BD_OPT_BATCH_KERNEL, 2), (bd.BD_OPT_BATCH_SINGLE, 1),
+                                        (bd.BD_OPT_TEST_STALL, 1), (bd.BD_OPT_PREFILL_KERNEL, 2),
+                                        (bd.BD_OPT_PAIR_RING, 2)])
+def test_options_accept_their_documented_range_only(lib, option, top):
+    prev = bd.bd_set_option(option, top)
+    try:
+        assert bd.bd_set_option(option, top + 1) == -1     # out of range: nothing changed
+        assert bd.bd_set_option(option, -1) == -1
+        assert bd.bd_set_option(option, 0) == top
+    finally:
+        bd.bd_set_option(option, prev)
+    assert bd.bd_set_option(0, 0) == -1 and bd.bd_set_option(99, 0) == -1  # unknown options
+
+
 def test_reconstruct_rejects_bad_arguments(lib):
     def rc(wb=ALIGNED, bits=ALIGNED, alpha=ALIGNED, mode=0, n_out=4, n_in=16, out=ALIGNED):
         return lib.bd_reconstruct(wb, bits, alpha, mode, n_out, n_in, out, None)

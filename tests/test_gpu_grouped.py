@@ -81,11 +81,13 @@ def test_uniform_ids_fourteen_variants(m):
     check_full(case, f"14 variants m={m}")
 
 
-@pytest.fixture(params=["single", "pair"])
+@pytest.fixture(params=["single", "pair5", "pair6"])
 def prefill_kernel(request):
     """The tensor-core kernel of the per-variant token tiles: one CTA per 128 W rows, or CTA pairs
-    on 256 W rows (BD_OPT_PREFILL_KERNEL)."""
-    with bd.option(bd.BD_OPT_PREFILL_KERNEL, 1 if request.param == "single" else 2):
+    on 256 W rows (BD_OPT_PREFILL_KERNEL) in either of the pair kernel's shapes (BD_OPT_PAIR_RING:
+    5-deep ring, whole tile staged; 6-deep ring, two staged halves)."""
+    kernel, ring = {"single": (1, 0), "pair5": (2, 1), "pair6": (2, 2)}[request.param]
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, kernel), bd.option(bd.BD_OPT_PAIR_RING, ring):
         yield request.param
 
 

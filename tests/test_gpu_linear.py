@@ -69,12 +69,15 @@ TENSOR_SHAPES = [  # ragged in every dimension: rows vs 128/256, tokens vs 256, 
     (1000, 2048, 263), (520, 4096, 1024),
 ]
 # the tensor-core kernels: one CTA per 128 x 256 tile, and CTA pairs on 256 x 256 tiles
-PREFILL_KERNELS = {"single": 1, "pair": 2}
+# (BD_OPT_PREFILL_KERNEL, BD_OPT_PAIR_RING): single-CTA tiles, and the CTA-pair kernel in both of
+# its shapes (5-deep ring with the whole output tile staged, 6-deep with two staged halves)
+PREFILL_KERNELS = {"single": (1, 0), "pair5": (2, 1), "pair6": (2, 2)}
 
 
 @pytest.fixture(params=list(PREFILL_KERNELS))
 def prefill_kernel(request):
-    with bd.option(bd.BD_OPT_PREFILL_KERNEL, PREFILL_KERNELS[request.param]):
+    kernel, ring = PREFILL_KERNELS[request.param]
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, kernel), bd.option(bd.BD_OPT_PAIR_RING, ring):
         yield request.param
 
 
@@ -85,13 +88,25 @@ def test_tensor_core_kernel_shapes(n_out, n_in, m, mode, prefill_kernel):
     full_check(case, TENSOR, f"tcgen05 {prefill_kernel} {n_out}x{n_in} m={m}")
 
 
+@pytest.mark.parametrize("ring", [1, 2])
+@pytest.mark.parametrize("n_out,n_in,m", [(8192, 72, 4096), (2000, 200, 3000), (4096, 8, 2048), (700, 1000, 5000)])
+def test_pair_kernel_many_tiles_per_pair(n_out, n_in, m, ring):
+    """The persistent pair kernel: several tiles per pair (up to ~7 here on 76 pairs), tiles of 1, 2,
+    4 or 16 K blocks so that tile boundaries fall at every position of the K-block ring, ragged W
+    rows and token tiles, both kernel shapes."""
+    case = LinearCase(n_out, n_in, m, 0.02, "row:5e-4:2e-3" if ring == 2 else 1e-3, ring - 1, seed=n_out + m)
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, 2), bd.option(bd.BD_OPT_PAIR_RING, ring):
+        full_check(case, TENSOR, f"pair ring {ring} {n_out}x{n_in} m={m}")
+
+
+@pytest.mark.parametrize("ring", [1, 2])
 @pytest.mark.parametrize("m", [1, 8, 9, 16, 17, 120, 128, 129, 255, 256])
-def test_pair_kernel_last_token_tile_split(m):
+def test_pair_kernel_last_token_tile_split(m, ring):
     """The pair's MMA N is the tile's token count rounded to 16, each CTA holding half of it:
     a last tile of few tokens leaves the odd CTA's half partly or wholly past the end."""
     case = LinearCase(300, 512, 256 + m, seed=40 + m)
-    with bd.option(bd.BD_OPT_PREFILL_KERNEL, 2):
-        full_check(case, TENSOR, f"pair m={256 + m}")
+    with bd.option(bd.BD_OPT_PREFILL_KERNEL, 2), bd.option(bd.BD_OPT_PAIR_RING, ring):
+        full_check(case, TENSOR, f"pair ring {ring} m={256 + m}")
 
 
 @pytest.mark.parametrize("path", [STREAM, STREAM_REG, TENSOR])

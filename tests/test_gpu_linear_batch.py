@@ -260,9 +260,11 @@ PAIR_BATCHES = {
 
 @pytest.mark.parametrize("name", list(PAIR_BATCHES))
 @pytest.mark.parametrize("mode", [0, 1])
-def test_tensor_core_problems_on_the_pair_kernel(name, mode):
+@pytest.mark.parametrize("ring", [0, 1, 2])
+def test_tensor_core_problems_on_the_pair_kernel(name, mode, ring):
     cases = make_cases(PAIR_BATCHES[name], seed0=700, mode=mode)
-    ys, ws = run_batch(cases)
+    with bd.option(bd.BD_OPT_PAIR_RING, ring):
+        ys, ws = run_batch(cases)
     check_all(cases, ys, f"pair batch {name} mode={mode}")
     assert_reusable(cases, ys, ws, f"pair batch {name}")
     # the same problems one by one on the pair kernel: identical bits
