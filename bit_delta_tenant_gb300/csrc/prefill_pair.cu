@@ -63,7 +63,6 @@ constexpr int kPN = 256;                  // tokens per pair tile (MMA N, at mos
 constexpr int kPK = 64;                   // K per stage: one 128-byte swizzle row of bf16
 constexpr uint32_t kPWBytes = kPM * kPK * 2;         // 16 KB
 constexpr uint32_t kPXBytes = (kPN / 2) * kPK * 2;   // 16 KB: this CTA's half of the tokens
-constexpr uint32_t kPStageTx = kPWBytes + kPXBytes;
 constexpr uint32_t kPAccCols = kPN;                  // fp32 accumulator columns (one per token)
 constexpr uint32_t kPTmemCols = 512;
 constexpr int kPRebuildWarps = 8;
@@ -105,9 +104,15 @@ struct PairLinear {
     int32_t first_pair;
 };
 
+// Token-operand boxes of 16, 32, 64 and 128 rows: a CTA loads the smallest box that holds
+// its half of the tile's MMA N, so tiles of few tokens (multi-tenant segments, a ragged
+// last token tile) do not pay for 128 rows.
+constexpr int kPXBoxes = 4;
+__host__ __device__ constexpr int x_box_rows(int i) { return 16 << i; }
+
 struct PairMaps {
-    CUtensorMap w[kPMaxLinears];  // W_base [n_out, n_in], boxes of 64 x 128 rows
-    CUtensorMap x[kPMaxLinears];  // x [m, n_in], boxes of 64 x 128 token rows
+    CUtensorMap w[kPMaxLinears];             // W_base [n_out, n_in], boxes of 64 x 128 rows
+    CUtensorMap x[kPMaxLinears][kPXBoxes];   // x [m, n_in], boxes of 64 x x_box_rows(i) token rows
 };
 
 struct PairArgs {
@@ -246,7 +251,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         mbar_fence_init();
         for (int i = 0; i < a.n_lin; ++i) {
             tma_prefetch_desc(&maps.w[i]);
-            tma_prefetch_desc(&maps.x[i]);
+            for (int b = 0; b < kPXBoxes; ++b) tma_prefetch_desc(&maps.x[i][b]);
         }
     }
     if (warp == 1) {
@@ -271,7 +276,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const int n_mma = (t.count + 15) & ~15;  // pair MMA N; each CTA holds n_mma / 2 token rows
                 const int m0 = t.row0 + static_cast<int>(rank) * kPM;
                 const int x_first = t.n0 + static_cast<int>(rank) * (n_mma / 2);
-                const CUtensorMap *tm_w = &maps.w[t.lp], *tm_x = &maps.x[t.lp];
+                const int bi = n_mma / 2 <= 16 ? 0 : n_mma / 2 <= 32 ? 1 : n_mma / 2 <= 64 ? 2 : 3;
+                const uint32_t tx = kPWBytes + static_cast<uint32_t>(x_box_rows(bi)) * (kPK * 2);
+                const CUtensorMap *tm_w = &maps.w[t.lp], *tm_x = &maps.x[t.lp][bi];
                 for (int kb = 0; kb < nkb; ++kb) {
                     const uint32_t s = g % kPStages;
                     const uint32_t ph = (g / kPStages) & 1;
@@ -280,7 +287,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], kPStageTx);
+                    mbar_arrive_expect_tx(&full[s], tx);
                     tma_load_2d(sW + s * kPWBytes, tm_w, &full[s], kb * kPK, m0);
                     tma_load_2d(sX + s * kPXBytes, tm_x, &full[s], kb * kPK, x_first);
                     ++g;
@@ -649,10 +656,14 @@ bool fill_linear(PairMaps &maps, PairArgs &a, int i, const void *x, int64_t x_ro
     L.bits_vec8 = ((n_in / 8) % 8 == 0 && (reinterpret_cast<uintptr_t>(bits) & 7) == 0) ? 1 : 0;
     L.y_vec16 = (n_out % 8 == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) ? 1 : 0;
     L.first_pair = first_pair;
-    return encode_tensor_map_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kPK,
-                                kPM, CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_tensor_map_2d(&maps.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, x_rows, n_in * 2, kPK,
-                                kPN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!encode_tensor_map_2d(&maps.w[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_base, n_in, n_out, n_in * 2, kPK,
+                              kPM, CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    for (int b = 0; b < kPXBoxes; ++b)
+        if (!encode_tensor_map_2d(&maps.x[i][b], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, n_in, x_rows, n_in * 2, kPK,
+                                  x_box_rows(b), CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+    return true;
 }
 
 }  // namespace
