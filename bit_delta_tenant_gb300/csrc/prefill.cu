@@ -545,12 +545,18 @@ cudaError_t launch_prefill_bn(const void *x, int64_t m, const void *w_base, cons
 cudaError_t launch_prefill(const void *x, int64_t m, const void *w_base, const uint8_t *bits, const float *alpha,
                            int32_t alpha_mode, int64_t n_out, int64_t n_in, void *y, const DevCtx &ctx,
                            cudaStream_t stream) {
-    // CTA pairs (256 x 256 tiles, half the activation traffic per SM) once their
-    // CTAs fill at least three quarters of the SMs; below that the single-CTA
-    // tiles, which can split K over a cluster to fill them.
+    // CTA pairs (256 x 256 tiles, half the activation traffic per SM) when their tiles
+    // fill at least 48 of the SMs' pairs (on 152 SMs: 5/8 of them), or at least 24 with
+    // m >= 256 and K <= 8192; otherwise the single-CTA tiles, which split K over a
+    // cluster to fill the SMs.  Measured on GB300 (single / pair, us): 14336 x 4096 at
+    // m = 256 (56 tiles) 44.2 / 37.2; 32 tiles: 4096^2 x 512 37.6 / 31.4, 1024 x 4096 x
+    // 2048 35.3 / 31.1, 8192^2 x 256 56.1 / 53.5, but 4096 x 14336 x 512 72.7 / 80.3 and
+    // 8192^2 x 128 45.7 / 49.5; 16 tiles: 4096^2 x 256 24.8 / 31.3.
     const int64_t forced = option_value(BD_OPT_PREFILL_KERNEL);
-    const bool pair = forced == 2 || (forced == 0 && m > 64 &&
-                                      8 * prefill_pair_tiles(m, n_out) >= 3 * static_cast<int64_t>(ctx.num_sms));
+    const int64_t tiles = prefill_pair_tiles(m, n_out);
+    const int64_t pairs = ctx.num_sms / 2;
+    const bool pair_auto = m > 64 && (8 * tiles >= 5 * pairs || (4 * tiles >= pairs && m >= 256 && n_in <= 8192));
+    const bool pair = forced == 2 || (forced == 0 && pair_auto);
     if (pair && prefill_pair_supported(m, n_out, n_in, ctx))
         return launch_prefill_pair(x, m, w_base, bits, alpha, alpha_mode, n_out, n_in, y, ctx, stream);
     if (m <= 64)
