@@ -60,6 +60,15 @@ def main():
         status_ok(f"linear {n_out}x{n_in} m={m} path {path}")
         y_ref, mag = case.reference()
         assert_y_close(y_host(y), y_ref, mag, f"linear {n_out}x{n_in} m={m}")
+    # the persistent pair kernel in both shapes (5-deep ring with the whole tile staged, 6-deep with two
+    # staged halves), several tiles per pair, ragged rows and tokens
+    for ring in (1, 2):
+        case = LinearCase(2000, 1000, 3000, mode=ring - 1, b="row:5e-4:2e-3" if ring == 2 else 1e-3, seed=40 + ring)
+        with bd.option(bd.BD_OPT_PREFILL_KERNEL, 2), bd.option(bd.BD_OPT_PAIR_RING, ring):
+            y = case.run_linear()
+        status_ok(f"pair kernel ring {ring}")
+        y_ref, mag = case.reference()
+        assert_y_close(y_host(y), y_ref, mag, f"pair kernel ring {ring}")
     # batched linear: the streaming batch kernels and a pair-kernel batch
     for shapes, kern in (([(200, 384, 3), (65, 1152, 8), (1000, 640, 2)], 2),
                          ([(200, 384, 3), (65, 1152, 8)], 1),
