@@ -99,6 +99,23 @@ def test_pair_kernel_many_tiles_per_pair(n_out, n_in, m, ring):
         full_check(case, TENSOR, f"pair ring {ring} {n_out}x{n_in} m={m}")
 
 
+@pytest.mark.parametrize("n_out,n_in,m,mode", [(3000, 1000, 2500, 1), (8192, 640, 1300, 0), (700, 8200, 600, 0)])
+def test_pair_kernel_shapes_give_identical_bits(n_out, n_in, m, mode):
+    """The pair kernel's two shapes differ only in ring depth and in how the output tile is staged,
+    not in the arithmetic or its order: their outputs are bit-identical (and match the oracle)."""
+    case = LinearCase(n_out, n_in, m, 0.02, "row:5e-4:2e-3" if mode else 1e-3, mode, seed=n_out + 3 * m)
+    ys = []
+    for ring in (1, 2):
+        with bd.option(bd.BD_OPT_PREFILL_KERNEL, 2), bd.option(bd.BD_OPT_PAIR_RING, ring):
+            ys.append(case.run_linear())
+    torch.cuda.synchronize()
+    assert bd.bd_get_device_status() == bd.BD_OK
+    assert torch.equal(ys[0], ys[1]), "the 5-deep and 6-deep shapes differ"
+    ts, js = sample_outputs(m, n_out, 600, seed=m)
+    y_ref, mag = case.reference_sampled(ts, js)
+    assert_y_close(y_host(ys[0])[ts, js], y_ref, mag, f"pair shapes {n_out}x{n_in} m={m}")
+
+
 @pytest.mark.parametrize("ring", [1, 2])
 @pytest.mark.parametrize("m", [1, 8, 9, 16, 17, 120, 128, 129, 255, 256])
 def test_pair_kernel_last_token_tile_split(m, ring):
